@@ -1,0 +1,181 @@
+"""Fused scaled-dot-product attention for GB300 (sm_103a): thin Python binding.
+
+Every function here only marshals arguments for libsdpa_gb300.so (C ABI in
+include/sdpa_gb300.h); all arithmetic runs in the library's CUDA kernels.
+PyTorch provides device memory and streams.  If the library is missing the
+calls raise: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "sdpa_prefill", "sdpa_decode", "prefill_workspace_bytes", "decode_workspace_bytes",
+    "device_status", "status_string", "library_path", "load_library", "SdpaError",
+    "EXPORTED_SYMBOLS",
+]
+
+SDPA_F16, SDPA_BF16 = 0, 1
+EXPORTED_SYMBOLS = ("sdpa_prefill", "sdpa_prefill_workspace_bytes", "sdpa_decode",
+                    "sdpa_decode_workspace_bytes", "sdpa_device_status", "sdpa_status_string",
+                    "sdpa_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SdpaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(path: str | None = None):
+    """Load (without building) the shared library and declare its signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        path = path or _build.LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: run attention_sm_flash_attn_gb300.build")
+        lib = ctypes.CDLL(path)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        attn = [vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, i, vp, sz, vp]
+        lib.sdpa_prefill.argtypes = attn
+        lib.sdpa_prefill.restype = i
+        lib.sdpa_decode.argtypes = attn
+        lib.sdpa_decode.restype = i
+        lib.sdpa_prefill_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
+        lib.sdpa_prefill_workspace_bytes.restype = sz
+        lib.sdpa_decode_workspace_bytes.argtypes = [i, i, i, i, i]
+        lib.sdpa_decode_workspace_bytes.restype = sz
+        lib.sdpa_device_status.argtypes = [vp, ctypes.POINTER(i)]
+        lib.sdpa_device_status.restype = i
+        lib.sdpa_status_string.argtypes = [i]
+        lib.sdpa_status_string.restype = ctypes.c_char_p
+        lib.sdpa_version.argtypes = []
+        lib.sdpa_version.restype = i
+        if path == _build.LIB_PATH:
+            _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load_library().sdpa_status_string(int(status)).decode()
+    except RuntimeError:
+        return "library not loaded"
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return SDPA_F16
+    if t.dtype == torch.bfloat16:
+        return SDPA_BF16
+    raise TypeError(f"only float16 / bfloat16 are supported, got {t.dtype}")
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _check(q, k, v, out):
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous [B, H, L, D]")
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be 4-D [B, H, L, D]")
+    if not (q.dtype == k.dtype == v.dtype == out.dtype):
+        raise TypeError("q, k, v, out must share one dtype")
+    B, Hq, Lq, D = q.shape
+    _, Hkv, Lk, _ = k.shape
+    if tuple(k.shape) != (B, Hkv, Lk, D) or tuple(v.shape) != (B, Hkv, Lk, D):
+        raise ValueError("k and v must be [B, Hkv, Lk, D] with q's B and D")
+    if tuple(out.shape) != tuple(q.shape):
+        raise ValueError("out must have q's shape")
+    return B, Hq, Hkv, Lq, Lk, D
+
+
+def prefill_workspace_bytes(B, Hq, Hkv, Lq, Lk, D, causal=False, window=0) -> int:
+    return int(load_library().sdpa_prefill_workspace_bytes(B, Hq, Hkv, Lq, Lk, D, int(causal),
+                                                           int(window)))
+
+
+def decode_workspace_bytes(B, Hq, Hkv, Lq, D) -> int:
+    return int(load_library().sdpa_decode_workspace_bytes(B, Hq, Hkv, Lq, D))
+
+
+def _workspace(nbytes: int, device, workspace):
+    if nbytes == 0:
+        return workspace
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return workspace
+
+
+def sdpa_prefill(q, k, v, out=None, *, scale=None, causal=False, window=0, workspace=None,
+                 stream=None):
+    """Fused attention over [B, H, L, D] fp16/bf16 CUDA tensors (see sdpa_prefill in
+    include/sdpa_gb300.h).  Returns ``out``.  ``workspace`` may be a uint8 CUDA
+    tensor; when None one is allocated with torch if the split plan wants it."""
+    if out is None:
+        out = torch.empty_like(q)
+    B, Hq, Hkv, Lq, Lk, D = _check(q, k, v, out)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    need = prefill_workspace_bytes(B, Hq, Hkv, Lq, Lk, D, causal, window)
+    workspace = _workspace(need, q.device, workspace)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = load_library().sdpa_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                      B, Hq, Hkv, Lq, Lk, D, float(scale), int(bool(causal)),
+                                      int(window), _dtype_code(q), ws_ptr, ws_len,
+                                      _stream_ptr(stream))
+    if rc != 0:
+        raise SdpaError(rc, "sdpa_prefill")
+    return out
+
+
+def sdpa_decode(q, k, v, out=None, *, scale=None, causal=True, window=0, workspace=None,
+                stream=None):
+    """Split-KV decode / verify for 1 <= Lq <= 8 (see sdpa_decode in
+    include/sdpa_gb300.h).  Returns ``out``."""
+    if out is None:
+        out = torch.empty_like(q)
+    B, Hq, Hkv, Lq, Lk, D = _check(q, k, v, out)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    need = decode_workspace_bytes(B, Hq, Hkv, Lq, D)
+    workspace = _workspace(need, q.device, workspace)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = load_library().sdpa_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                     B, Hq, Hkv, Lq, Lk, D, float(scale), int(bool(causal)),
+                                     int(window), _dtype_code(q), ws_ptr, ws_len,
+                                     _stream_ptr(stream))
+    if rc != 0:
+        raise SdpaError(rc, "sdpa_decode")
+    return out
+
+
+def device_status(stream=None):
+    """(status, detail): synchronises the stream and reads/clears the device status word."""
+    detail = ctypes.c_int(0)
+    rc = load_library().sdpa_device_status(_stream_ptr(stream), ctypes.byref(detail))
+    return int(rc), int(detail.value)

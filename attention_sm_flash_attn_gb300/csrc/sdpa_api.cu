@@ -1,0 +1,360 @@
+// sdpa_api.cu -- host side of libsdpa_gb300.so: argument validation, TMA
+// descriptor encoding, work planning and launches.  The C ABI is declared in
+// include/sdpa_gb300.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <cstdint>
+#include <mutex>
+
+#include "sdpa_gb300.h"
+#include "sdpa_kernels.cuh"
+
+namespace {
+
+using gbsdpa::AttnParams;
+using gbsdpa::Cfg;
+
+__device__ int g_device_status;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  int* status = nullptr;  // device address of g_device_status
+  bool attr_set[4] = {false, false, false, false};
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SDPA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return SDPA_ERR_CUDA;
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) return SDPA_ERR_CUDA;
+    st.status = static_cast<int*>(addr);
+    if (!g_encode) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return SDPA_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    st.ready = true;
+  }
+  *out = &st;
+  return SDPA_OK;
+}
+
+// 3-D map over a contiguous [BH, L, D] tensor: dims (D, L, BH), box (64, rows, 1),
+// 128-byte swizzle; rows past L read as zero and never spill into the next head.
+int encode_map(CUtensorMap* m, const void* base, int D, long long L, long long BH, int rows,
+               bool bf16) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                           static_cast<cuuint64_t>(L) * static_cast<cuuint64_t>(D) * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        3, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int validate(const void* q, const void* k, const void* v, const void* out, int B, int Hq, int Hkv,
+             int Lq, int Lk, int D, float scale, int causal, int window, int dtype) {
+  if (!q || !k || !v || !out) return SDPA_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lk <= 0) return SDPA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return SDPA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return SDPA_ERR_INVALID_ARG;
+  if (window < 0 || (window > 0 && !causal)) return SDPA_ERR_INVALID_ARG;
+  if (causal && Lq > Lk) return SDPA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.f) return SDPA_ERR_INVALID_ARG;
+  if (D != 256 && D != 512) return SDPA_ERR_UNSUPPORTED;
+  if (dtype != SDPA_F16 && dtype != SDPA_BF16) return SDPA_ERR_UNSUPPORTED;
+  // TMA coordinates and flat row indices stay within 32-bit / 64-bit ranges.
+  if (static_cast<long long>(B) * Hq > (1ll << 30) || static_cast<long long>(B) * Hkv > (1ll << 30))
+    return SDPA_ERR_INVALID_ARG;
+  if (Lk > (1 << 30) || Lq > (1 << 30)) return SDPA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return SDPA_ERR_ALIGNMENT;
+  return SDPA_OK;
+}
+
+template <bool BF16, bool PAIR>
+int ensure_attr(DeviceState* st) {
+  const int idx = (BF16 ? 1 : 0) + (PAIR ? 2 : 0);
+  if (st->attr_set[idx]) return SDPA_OK;
+  auto kern = gbsdpa::attn_fwd_kernel<BF16, PAIR>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<BF16, PAIR>::SMEM_BYTES) != cudaSuccess)
+    return SDPA_ERR_CUDA;
+  st->attr_set[idx] = true;
+  return SDPA_OK;
+}
+
+template <bool BF16, bool PAIR>
+int launch_attn(const AttnParams& p, long long items, cudaStream_t stream, DeviceState* st) {
+  int rc = ensure_attr<BF16, PAIR>(st);
+  if (rc) return rc;
+  const long long ctas = items * (PAIR ? 2 : 1);
+  if (ctas <= 0 || ctas > 0x7fffffffll) return SDPA_ERR_INVALID_ARG;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<BF16, PAIR>::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (PAIR) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gbsdpa::attn_fwd_kernel<BF16, PAIR>, p);
+  return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+int launch_combine(const float* part_o, const float* part_ml, void* out, long long R, int D,
+                   int n_splits, bool bf16, cudaStream_t stream) {
+  const size_t sh = static_cast<size_t>(n_splits + 1) * sizeof(float);
+  if (R <= 0 || R > 0x7fffffffll) return SDPA_ERR_INVALID_ARG;
+  if (bf16)
+    gbsdpa::combine_kernel<true><<<static_cast<unsigned>(R), 128, sh, stream>>>(
+        part_o, part_ml, static_cast<uint16_t*>(out), R, D, n_splits);
+  else
+    gbsdpa::combine_kernel<false><<<static_cast<unsigned>(R), 128, sh, stream>>>(
+        part_o, part_ml, static_cast<uint16_t*>(out), R, D, n_splits);
+  return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+size_t partial_bytes(long long R, int D, int n_splits) {
+  // part_o then part_ml, each 256-byte aligned.
+  const size_t po = static_cast<size_t>(n_splits) * static_cast<size_t>(R) * D * sizeof(float);
+  const size_t pm = static_cast<size_t>(n_splits) * static_cast<size_t>(R) * 2 * sizeof(float);
+  return ((po + 255) & ~static_cast<size_t>(255)) + ((pm + 255) & ~static_cast<size_t>(255));
+}
+
+// Key tiles (of `bn` keys) the longest 128-row query tile visits.
+long long max_tiles_per_qtile(int Lq, int Lk, int causal, int window, int bn) {
+  const int m0 = ((Lq - 1) / 128) * 128;  // last query tile sees the most keys when causal
+  const int pmin = Lk - Lq + m0, pmax = Lk - 1;
+  const int lo = (causal && window) ? std::max(0, pmin - window + 1) : 0;
+  const int hi = causal ? std::min(Lk, pmax + 1) : Lk;
+  if (!causal) return (Lk + bn - 1) / bn;
+  (void)pmin;
+  return (hi + bn - 1) / bn - lo / bn;
+}
+
+// How many contiguous shares to cut each query tile's key range into.  A
+// simple wave model: time ~ ceil(ctas / sms) * ceil(tiles / s), plus the cost
+// of writing and re-reading the fp32 partials.
+int plan_prefill_splits(int sms, int B, int Hq, int Lq, int Lk, int D, int causal, int window) {
+  const bool pair = D == 512;
+  const int bn = pair ? 64 : 128;
+  const long long items = static_cast<long long>(B) * Hq * ((Lq + 127) / 128);
+  const long long per_cta = pair ? 2 : 1;
+  const long long slots = std::max<long long>(1, sms / per_cta);
+  const long long T = max_tiles_per_qtile(Lq, Lk, causal, window, bn);
+  if (items >= 2 * slots || T < 16) return 1;
+  // one key tile ~ 4 * 128 * bn * 256 flop per CTA at ~8 Kflop/clk, ~1.9 GHz
+  const double t_tile_us = 4.0 * 128 * bn * 256 / 8192.0 / 1900.0;
+  const double partial_us_per_split =
+      static_cast<double>(B) * Hq * Lq * D * 4.0 * 2.0 / 6.0e6;  // write + read at ~6 TB/s
+  int best = 1;
+  double best_t = 1e300;
+  for (int s = 1; s <= 8; ++s) {
+    const long long waves = (items * s + slots - 1) / slots;
+    const double t = waves * ((T + s - 1) / s) * t_tile_us + (s > 1 ? s * partial_us_per_split : 0);
+    if (t < best_t * 0.97) {
+      best_t = t;
+      best = s;
+    }
+  }
+  return best;
+}
+
+int plan_decode_splits(int sms, int B, int Hq, int Hkv, int D) {
+  const int G = Hq / Hkv;
+  const long long n_hb = (G + 15) / 16;
+  const long long per_cta = D == 512 ? 2 : 1;
+  const long long units = static_cast<long long>(B) * Hkv * n_hb * per_cta;
+  long long s = sms / std::max<long long>(1, units);
+  s = std::max<long long>(1, std::min<long long>(s, 256));
+  return static_cast<int>(s);
+}
+
+template <bool BF16>
+int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv, int Lq,
+        int Lk, int D, float scale, int causal, int window, bool decode, int n_splits,
+        bool write_partial, void* workspace, cudaStream_t stream, DeviceState* st) {
+  AttnParams p;
+  std::memset(&p, 0, sizeof(p));
+  const bool pair = D == 512;
+  const int bn = pair ? 64 : 128;
+  int rc = SDPA_OK;
+  if (!decode) rc = encode_map(&p.tm_q, q, D, Lq, static_cast<long long>(B) * Hq, 128, BF16);
+  if (rc) return rc;
+  rc = encode_map(&p.tm_k, k, D, Lk, static_cast<long long>(B) * Hkv, bn, BF16);
+  if (rc) return rc;
+  rc = encode_map(&p.tm_v, v, D, Lk, static_cast<long long>(B) * Hkv, 32, BF16);
+  if (rc) return rc;
+  const long long R = static_cast<long long>(B) * Hq * Lq;
+  p.q = static_cast<const uint16_t*>(q);
+  p.out = static_cast<uint16_t*>(out);
+  if (write_partial) {
+    const size_t po = static_cast<size_t>(n_splits) * static_cast<size_t>(R) * D * sizeof(float);
+    p.part_o = static_cast<float*>(workspace);
+    p.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                         ((po + 255) & ~static_cast<size_t>(255)));
+  }
+  p.status = st->status;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.D = D;
+  p.causal = causal;
+  p.window = window;
+  p.c = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.decode = decode ? 1 : 0;
+  p.n_qtiles = (Lq + 127) / 128;
+  p.n_splits = n_splits;
+  p.n_hb = (p.G + 15) / 16;
+  p.write_partial = write_partial ? 1 : 0;
+  long long items;
+  if (decode)
+    items = static_cast<long long>(B) * Hkv * n_splits * p.n_hb;
+  else
+    items = static_cast<long long>(B) * Hq * p.n_qtiles * n_splits;
+  rc = pair ? launch_attn<BF16, true>(p, items, stream, st)
+            : launch_attn<BF16, false>(p, items, stream, st);
+  if (rc) return rc;
+  if (write_partial)
+    rc = launch_combine(p.part_o, p.part_ml, out, R, D, n_splits, BF16, stream);
+  return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t sdpa_prefill_workspace_bytes(int B, int Hq, int Hkv, int Lq, int Lk, int D, int causal,
+                                    int window) {
+  DeviceState* st = nullptr;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lk <= 0 || Hq % Hkv) return 0;
+  if (D != 256 && D != 512) return 0;
+  if (device_state(&st)) return 0;
+  const int s = plan_prefill_splits(st->sms, B, Hq, Lq, Lk, D, causal, window);
+  if (s <= 1) return 0;
+  return partial_bytes(static_cast<long long>(B) * Hq * Lq, D, s);
+}
+
+size_t sdpa_decode_workspace_bytes(int B, int Hq, int Hkv, int Lq, int D) {
+  DeviceState* st = nullptr;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lq > 8 || Hq % Hkv) return 0;
+  if (D != 256 && D != 512) return 0;
+  if (device_state(&st)) return 0;
+  const int s = plan_decode_splits(st->sms, B, Hq, Hkv, D);
+  return partial_bytes(static_cast<long long>(B) * Hq * Lq, D, s);
+}
+
+int sdpa_prefill(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
+                 int Lq, int Lk, int D, float scale, int causal, int window, int dtype,
+                 void* workspace, size_t workspace_bytes, sdpa_stream_t stream) {
+  int rc = validate(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, dtype);
+  if (rc) return rc;
+  if (workspace && !aligned16(workspace)) return SDPA_ERR_ALIGNMENT;
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc) return rc;
+  int s = plan_prefill_splits(st->sms, B, Hq, Lq, Lk, D, causal, window);
+  if (s > 1 && (!workspace ||
+                workspace_bytes < partial_bytes(static_cast<long long>(B) * Hq * Lq, D, s)))
+    s = 1;
+  const bool bf16 = dtype == SDPA_BF16;
+  auto strm = reinterpret_cast<cudaStream_t>(stream);
+  return bf16 ? run<true>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, false, s,
+                          s > 1, workspace, strm, st)
+              : run<false>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, false, s,
+                           s > 1, workspace, strm, st);
+}
+
+int sdpa_decode(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
+                int Lq, int Lk, int D, float scale, int causal, int window, int dtype,
+                void* workspace, size_t workspace_bytes, sdpa_stream_t stream) {
+  int rc = validate(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, dtype);
+  if (rc) return rc;
+  if (Lq > 8) return SDPA_ERR_INVALID_ARG;
+  if (!workspace) return SDPA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return SDPA_ERR_ALIGNMENT;
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc) return rc;
+  const int s = plan_decode_splits(st->sms, B, Hq, Hkv, D);
+  if (workspace_bytes < partial_bytes(static_cast<long long>(B) * Hq * Lq, D, s))
+    return SDPA_ERR_WORKSPACE;
+  const bool bf16 = dtype == SDPA_BF16;
+  auto strm = reinterpret_cast<cudaStream_t>(stream);
+  return bf16 ? run<true>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, true, s,
+                          true, workspace, strm, st)
+              : run<false>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, true, s,
+                           true, workspace, strm, st);
+}
+
+int sdpa_device_status(sdpa_stream_t stream, int* detail) {
+  DeviceState* st = nullptr;
+  if (detail) *detail = 0;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  auto strm = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(strm) != cudaSuccess) return SDPA_ERR_CUDA;
+  int code = 0;
+  if (cudaMemcpy(&code, st->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SDPA_ERR_CUDA;
+  if (code) {
+    const int zero = 0;
+    if (cudaMemcpy(st->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return SDPA_ERR_CUDA;
+  }
+  if (detail) *detail = code;
+  return code ? SDPA_ERR_DEVICE_TIMEOUT : SDPA_OK;
+}
+
+const char* sdpa_status_string(int status) {
+  switch (status) {
+    case SDPA_OK: return "ok";
+    case SDPA_ERR_INVALID_ARG: return "invalid argument";
+    case SDPA_ERR_UNSUPPORTED: return "unsupported head dim or dtype";
+    case SDPA_ERR_WORKSPACE: return "workspace missing or too small";
+    case SDPA_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case SDPA_ERR_DEVICE_TIMEOUT: return "a kernel wait gave up (device timeout)";
+    case SDPA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    default: return "unknown status";
+  }
+}
+
+int sdpa_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,737 @@
+// sdpa_kernels.cuh -- fused scaled-dot-product attention kernels for sm_103a.
+//
+// What is computed (the unfused "matmul + softmax + matmul" of the page
+// "fix: add head_dim=256 to fused SDPA full attention kernel", section
+// "Benchmark: fused vs unfused SDPA for head_dim=256", done tile by tile so the
+// [heads, Lq, Lk] score matrix never exists):
+//
+//   for query row i of head h (kv head g = h / G, G = Hq / Hkv), position
+//   p = Lk - Lq + i (bottom-right aligned), visible keys j with
+//   (!causal || j <= p) && (window == 0 || p - j < window):
+//     out[h, i] = sum_j softmax_j(scale * q_i . k_j) v_j
+//
+// One CTA owns 128 query rows (one tcgen05 M=128 tile) and walks a list of
+// key tiles.  Warp roles:
+//   warps 0-3  softmax + epilogue: one thread per row / TMEM lane
+//   warp  4    TMA producer: Q once, then K and V sub-tiles into a ring
+//   warp  5    TMEM allocator and tcgen05.mma issuer
+// Per key tile j:  S_j = Q K_j^T (tcgen05, fp32 in TMEM, double buffered)
+//                  softmax warps: tcgen05.ld S_j, mask, online max/sum (log2
+//                  domain, lazy rescale), P_j -> shared memory (fp16/bf16)
+//                  O += P_j V_j  (tcgen05, fp32 in TMEM)
+// Whole key tiles outside the causal/window band are never visited.
+//
+// Modes:
+//  * prefill: 128 consecutive query rows of one head; either the whole visible
+//    key range (final output) or one contiguous share of it (fp32 partials
+//    merged by the combine kernel);
+//  * decode (Lq <= 8): the 128 rows are 16 query heads x 8 slots of one kv
+//    head; query row i goes to slot (p_i mod 8), so the same row always lands
+//    on the same TMEM lane whatever Lq is.  Key tiles are dealt round-robin
+//    over a fixed number of splits, so the arithmetic one row sees does not
+//    depend on how many query rows share the call ("fix: Gemma 4 MTP never
+//    engages on CUDA (GB10)", sections "Proposed Solution" and "Acceptance
+//    Criteria": a verify row must be byte-identical to the single-row call).
+//  * PAIR (head_dim 512): a 2-CTA cluster splits the head dimension; each CTA
+//    forms its half of the scores, the halves are swapped through distributed
+//    shared memory and summed (both CTAs add the same two fp32 numbers, so
+//    both run an identical softmax), then each CTA accumulates its half of O.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace gbsdpa {
+
+// Device status codes (bit pattern identifies the wait that gave up).
+enum : int {
+  kDevOk = 0,
+  kDevTimeoutQ = 0x100,
+  kDevTimeoutKvFull = 0x101,
+  kDevTimeoutKvEmpty = 0x102,
+  kDevTimeoutSFull = 0x103,
+  kDevTimeoutSEmpty = 0x104,
+  kDevTimeoutPFull = 0x105,
+  kDevTimeoutPvDone = 0x106,
+  kDevTimeoutXFull = 0x107,
+  kDevTimeoutXFree = 0x108,
+  kDevTimeoutDrain = 0x109,
+};
+
+struct AttnParams {
+  CUtensorMap tm_q;  // (D, Lq, B*Hq) box (64, 128, 1), 128B swizzle
+  CUtensorMap tm_k;  // (D, Lk, B*Hkv) box (64, BN, 1)
+  CUtensorMap tm_v;  // (D, Lk, B*Hkv) box (64, 32, 1)
+  const uint16_t* q;
+  uint16_t* out;
+  float* part_o;   // [n_splits][B*Hq*Lq][D]
+  float* part_ml;  // [n_splits][B*Hq*Lq][2]  (running max in log2 units, sum)
+  int* status;
+  int B, Hq, Hkv, G, Lq, Lk, D;
+  int causal, window;
+  float c;        // scale * log2(e)
+  int decode;     // 0 = prefill, 1 = decode
+  int n_qtiles;   // prefill: ceil(Lq / 128)
+  int n_splits;   // prefill: 1 => final output written directly; decode: fixed split count
+  int n_hb;       // decode: query-head blocks of 16 per kv head
+  int write_partial;
+};
+
+template <bool BF16, bool PAIR>
+struct Cfg {
+  static constexpr int BM = 128;
+  static constexpr int DH = 256;  // head-dim columns owned by one CTA
+  static constexpr int BN = PAIR ? 64 : 128;
+  static constexpr int NSLOT = PAIR ? 7 : 8;
+  static constexpr int SLOT = 16384;
+  static constexpr int KSUB = DH * BN * 2 / SLOT;   // K sub-tiles per key tile
+  static constexpr int KBOX = SLOT / (BN * 128);    // 64-column boxes per K sub-tile
+  static constexpr int VSUB = BN / 32;              // V sub-tiles (32 keys x 256 cols)
+  static constexpr int Q_OFF = 0;
+  static constexpr int RING_OFF = 65536;
+  static constexpr int P_OFF = RING_OFF + NSLOT * SLOT;
+  static constexpr int P_BYTES = BM * BN * 2;
+  static constexpr int X_OFF = P_OFF + P_BYTES;
+  static constexpr int X_BYTES = PAIR ? BM * BN * 4 : 0;
+  static constexpr int BAR_OFF = X_OFF + X_BYTES;
+  static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
+  static constexpr int S_COL = 256;  // TMEM: O in columns [0,256), S buffers after it
+  static constexpr uint32_t IDESC_QK = ptx::idesc_f16(128, BN, BF16, false, false);
+  static constexpr uint32_t IDESC_PV = ptx::idesc_f16(128, DH, BF16, false, true);
+  static_assert(S_COL + 2 * BN <= 512, "TMEM budget");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+// Barrier slots inside the barrier area.
+enum {
+  kBarQ = 0,
+  kBarKvFull = 1,    // + slot (8 slots max)
+  kBarKvEmpty = 9,   // + slot
+  kBarSFull = 17,    // + buf
+  kBarSEmpty = 19,   // + buf
+  kBarPFull = 21,
+  kBarPvDone = 22,
+  kBarXFull = 23,
+  kBarXFree = 24,
+  kBarDrain = 25,
+  kNumBars = 26,
+};
+
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
+
+// Bounded mbarrier wait.  Gives up after kTimeoutNs (or when another role of
+// this CTA already gave up), records `code` in the device status word and
+// returns false.
+template <bool kCluster = false>
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         int* status, int code) {
+  if (kCluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity))
+    return true;
+  const uint64_t t0 = ptx::globaltimer();
+  for (uint32_t n = 1; n < (1u << 26); ++n) {
+    if (kCluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity))
+      return true;
+    if ((n & 63) == 0) {
+      if (*abort_flag) return false;
+      if (ptx::globaltimer() - t0 > kTimeoutNs) break;
+    }
+  }
+  *abort_flag = 1;
+  atomicCAS(status, 0, code);
+  return false;
+}
+
+struct Work {
+  int b, hkv, h0;      // batch, kv head, first query head of the CTA
+  int split;
+  int m0;              // prefill: first query row
+  int pmin, pmax;      // positions spanned by the CTA's rows
+  int t_begin, t_step, t_count;
+};
+
+template <int BN>
+__device__ __forceinline__ Work make_work(const AttnParams& p, int item) {
+  Work w;
+  int lo, hi;
+  if (!p.decode) {
+    const int hl = item % p.G;
+    item /= p.G;
+    w.split = item % p.n_splits;
+    item /= p.n_splits;
+    w.hkv = item % p.Hkv;
+    item /= p.Hkv;
+    w.b = item % p.B;
+    item /= p.B;
+    const int qt = p.n_qtiles - 1 - item;  // longest causal tiles first
+    w.h0 = w.hkv * p.G + hl;
+    w.m0 = qt * 128;
+    const int mlast = min(w.m0 + 128, p.Lq) - 1;
+    w.pmin = p.Lk - p.Lq + w.m0;
+    w.pmax = p.Lk - p.Lq + mlast;
+    lo = (p.causal && p.window) ? max(0, w.pmin - p.window + 1) : 0;
+    hi = p.causal ? min(p.Lk, w.pmax + 1) : p.Lk;
+    const int tlo = lo / BN, thi = (hi + BN - 1) / BN;
+    const int per = (thi - tlo + p.n_splits - 1) / p.n_splits;
+    w.t_begin = tlo + w.split * per;
+    w.t_step = 1;
+    w.t_count = max(0, min(per, thi - w.t_begin));
+  } else {
+    const int hb = item % p.n_hb;
+    item /= p.n_hb;
+    w.split = item % p.n_splits;
+    item /= p.n_splits;
+    w.hkv = item % p.Hkv;
+    w.b = item / p.Hkv;
+    w.h0 = w.hkv * p.G + hb * 16;
+    w.m0 = 0;
+    w.pmin = p.Lk - p.Lq;
+    w.pmax = p.Lk - 1;
+    lo = (p.causal && p.window) ? max(0, w.pmin - p.window + 1) : 0;
+    hi = p.Lk;
+    const int tlo = lo / BN, thi = (hi + BN - 1) / BN;
+    const int S = p.n_splits;
+    const int t0 = tlo + (((w.split - tlo) % S) + S) % S;
+    w.t_begin = t0;
+    w.t_step = S;
+    w.t_count = t0 < thi ? (thi - 1 - t0) / S + 1 : 0;
+  }
+  return w;
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
+  if (bf16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+template <bool BF16, bool PAIR>
+__global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
+  using C = Cfg<BF16, PAIR>;
+  constexpr int BN = C::BN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  const uint32_t sQ = sbase + C::Q_OFF;
+  const uint32_t sRing = sbase + C::RING_OFF;
+  const uint32_t sP = sbase + C::P_OFF;
+  const uint32_t sX = sbase + C::X_OFF;
+  const uint32_t sBar = sbase + C::BAR_OFF;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::BAR_OFF + 224);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 228);
+  auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
+  const int item = PAIR ? static_cast<int>(blockIdx.x / 2) : static_cast<int>(blockIdx.x);
+  const Work w = make_work<BN>(p, item);
+  const int d0 = static_cast<int>(rank) * C::DH;  // head-dim offset of this CTA
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(kBarQ), 1);
+    for (int s = 0; s < C::NSLOT; ++s) {
+      ptx::mbar_init(bar(kBarKvFull + s), 1);
+      ptx::mbar_init(bar(kBarKvEmpty + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(bar(kBarSFull + b), 1);
+      ptx::mbar_init(bar(kBarSEmpty + b), 128);
+    }
+    ptx::mbar_init(bar(kBarPFull), 128);
+    ptx::mbar_init(bar(kBarPvDone), 1);
+    ptx::mbar_init(bar(kBarXFull), 128);
+    ptx::mbar_init(bar(kBarXFree), 128);
+    ptx::mbar_init(bar(kBarDrain), 1);
+    *abort_flag = 0;
+    ptx::fence_mbarrier_init();
+  }
+  if (warp == 4 && lane == 0 && !p.decode) {
+    ptx::prefetch_tmap(&p.tm_q);
+    ptx::prefetch_tmap(&p.tm_k);
+    ptx::prefetch_tmap(&p.tm_v);
+  }
+  if (warp == 5) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (PAIR) ptx::cluster_sync();  // peer barriers initialised before any remote arrive
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int count = w.t_count;
+
+  // Producer / MMA bookkeeping kept for the drain after an abort.
+  int issued_q = 0;
+  uint32_t ring_issued = 0;  // ring loads issued, in sequence order
+  int mma_issued = 0;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && count > 0) {
+      const int bh_q = w.b * p.Hq + w.h0;
+      const int bh_kv = w.b * p.Hkv + w.hkv;
+      if (!p.decode) {
+        ptx::mbar_arrive_expect_tx(bar(kBarQ), 65536);
+        for (int c = 0; c < 4; ++c)
+          ptx::tma_load_3d(sQ + c * 16384, &p.tm_q, bar(kBarQ), d0 + c * 64, w.m0, bh_q);
+        issued_q = 1;
+      }
+      uint32_t n = 0;  // ring sequence number
+      bool ok = true;
+      auto load_k = [&](int j) {
+        const int key0 = (w.t_begin + j * w.t_step) * BN;
+        for (int ks = 0; ks < C::KSUB && ok; ++ks, ++n) {
+          const int slot = n % C::NSLOT;
+          if (!wait_bar(bar(kBarKvEmpty + slot), ((n / C::NSLOT) & 1) ^ 1, abort_flag, p.status,
+                        kDevTimeoutKvEmpty)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(bar(kBarKvFull + slot), C::SLOT);
+          for (int e = 0; e < C::KBOX; ++e)
+            ptx::tma_load_3d(sRing + slot * C::SLOT + e * (BN * 128), &p.tm_k,
+                             bar(kBarKvFull + slot), d0 + (ks * C::KBOX + e) * 64, key0, bh_kv);
+          ring_issued = n + 1;
+        }
+      };
+      auto load_v = [&](int j) {
+        const int key0 = (w.t_begin + j * w.t_step) * BN;
+        for (int vs = 0; vs < C::VSUB && ok; ++vs, ++n) {
+          const int slot = n % C::NSLOT;
+          if (!wait_bar(bar(kBarKvEmpty + slot), ((n / C::NSLOT) & 1) ^ 1, abort_flag, p.status,
+                        kDevTimeoutKvEmpty)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(bar(kBarKvFull + slot), C::SLOT);
+          for (int c = 0; c < 4; ++c)
+            ptx::tma_load_3d(sRing + slot * C::SLOT + c * 4096, &p.tm_v, bar(kBarKvFull + slot),
+                             d0 + c * 64, key0 + vs * 32, bh_kv);
+          ring_issued = n + 1;
+        }
+      };
+      load_k(0);
+      for (int j = 1; j < count && ok; ++j) {
+        load_k(j);
+        load_v(j - 1);
+      }
+      if (ok) load_v(count - 1);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && count > 0) {
+      bool ok = wait_bar(bar(kBarQ), 0, abort_flag, p.status, kDevTimeoutQ);
+      ptx::tc_fence_after();
+      uint32_t n = 0;
+      auto consume = [&](uint32_t& slot_addr) -> bool {
+        const int slot = n % C::NSLOT;
+        if (!wait_bar(bar(kBarKvFull + slot), (n / C::NSLOT) & 1, abort_flag, p.status,
+                      kDevTimeoutKvFull))
+          return false;
+        ptx::tc_fence_after();
+        slot_addr = sRing + slot * C::SLOT;
+        return true;
+      };
+      auto release = [&]() {
+        ptx::mma_commit(bar(kBarKvEmpty + (n % C::NSLOT)));
+        ++n;
+      };
+      auto do_s = [&](int j) {
+        const int buf = j & 1;
+        if (!wait_bar(bar(kBarSEmpty + buf), ((j >> 1) & 1) ^ 1, abort_flag, p.status,
+                      kDevTimeoutSEmpty)) {
+          ok = false;
+          return;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem + C::S_COL + buf * BN;
+        for (int ks = 0; ks < C::KSUB; ++ks) {
+          uint32_t sk;
+          if (!consume(sk)) {
+            ok = false;
+            return;
+          }
+#pragma unroll
+          for (int e = 0; e < C::KBOX; ++e) {
+            const int dc = ks * C::KBOX + e;  // 64-column chunk of the head dim
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t a = ptx::sdesc_sw128(sQ + dc * 16384 + kk * 32, 16, 1024);
+              const uint64_t b = ptx::sdesc_sw128(sk + e * (BN * 128) + kk * 32, 16, 1024);
+              ptx::mma_f16_ss(d_tmem, a, b, C::IDESC_QK, (dc | kk) != 0);
+            }
+          }
+          release();
+          ++mma_issued;
+        }
+        ptx::mma_commit(bar(kBarSFull + buf));
+      };
+      auto do_pv = [&](int j) {
+        if (!wait_bar(bar(kBarPFull), j & 1, abort_flag, p.status, kDevTimeoutPFull)) {
+          ok = false;
+          return;
+        }
+        ptx::tc_fence_after();
+        for (int vs = 0; vs < C::VSUB; ++vs) {
+          uint32_t sv;
+          if (!consume(sv)) {
+            ok = false;
+            return;
+          }
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            const int key = vs * 32 + kk * 16;
+            const uint64_t a =
+                ptx::sdesc_sw128(sP + (key / 64) * 16384 + (key % 64) * 2, 16, 1024);
+            const uint64_t b = ptx::sdesc_sw128(sv + kk * 2048, 4096, 1024);
+            ptx::mma_f16_ss(tmem, a, b, C::IDESC_PV, (j | vs | kk) != 0);
+          }
+          release();
+          ++mma_issued;
+        }
+        ptx::mma_commit(bar(kBarPvDone));
+      };
+      if (ok) do_s(0);
+      for (int j = 1; j < count && ok; ++j) {
+        do_s(j);
+        if (ok) do_pv(j - 1);
+      }
+      if (ok) do_pv(count - 1);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int t = threadIdx.x;  // row of the tile == TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    // Row identity.
+    int row_p;            // bottom-right position of this row
+    bool row_valid;
+    long long row_id;     // flat (b, h, i) row index, -1 if none
+    if (!p.decode) {
+      const int i = w.m0 + t;
+      row_valid = i < p.Lq;
+      row_p = p.Lk - p.Lq + min(i, p.Lq - 1);
+      row_id = row_valid ? (static_cast<long long>(w.b) * p.Hq + w.h0) * p.Lq + i : -1;
+    } else {
+      const int hl = t >> 3;
+      const int slot = t & 7;
+      const int base = p.Lk - p.Lq;
+      const int i = (((slot - base) % 8) + 8) % 8;
+      const int h = w.h0 + hl;
+      row_valid = (i < p.Lq) && (hl < min(p.G, 16)) && (h < (w.hkv + 1) * p.G);
+      row_p = base + (row_valid ? i : 0);
+      row_id = row_valid ? (static_cast<long long>(w.b) * p.Hq + h) * p.Lq + i : -1;
+      if (count > 0) {
+        // Decode: stage this row's query slice into the swizzled Q tile.
+        const uint4* src = reinterpret_cast<const uint4*>(p.q + row_id * p.D + d0);
+        for (int c = 0; c < C::DH / 8; ++c) {  // 16-byte chunks of 8 elements
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (row_valid) v = src[c];
+          const int dc = c >> 3, cc = c & 7;
+          const uint32_t addr = sQ + dc * 16384 + t * 128 + ((cc ^ (t & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x),
+                       "r"(v.y), "r"(v.z), "r"(v.w)
+                       : "memory");
+        }
+        ptx::fence_proxy_async_smem();
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (t == 0) ptx::mbar_arrive(bar(kBarQ));
+      }
+    }
+
+    const float c = p.c;
+    float m_run = -INFINITY;  // running max of scale*log2e*s (lazy: may lag by < 8)
+    float l = 0.f;
+    bool ok = true;
+    const uint32_t peer = rank ^ 1u;
+
+    for (int j = 0; j < count && ok; ++j) {
+      const int tile = w.t_begin + j * w.t_step;
+      const int kb = tile * BN;
+      const int buf = j & 1;
+      ok = __all_sync(0xffffffffu,
+                      wait_bar(bar(kBarSFull + buf), (j >> 1) & 1, abort_flag, p.status,
+                               kDevTimeoutSFull));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      float s[BN];
+      {
+        uint32_t r[BN / 32][32];
+#pragma unroll
+        for (int cch = 0; cch < BN / 32; ++cch)
+          ptx::tmem_ld32(lane_base + C::S_COL + buf * BN + cch * 32, r[cch]);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int cch = 0; cch < BN / 32; ++cch) {
+          ptx::reg_fence(r[cch]);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) s[cch * 32 + e] = __uint_as_float(r[cch][e]);
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(kBarSEmpty + buf));
+
+      if constexpr (PAIR) {
+        // Swap partial scores with the peer CTA and add them.
+        ok = __all_sync(0xffffffffu, wait_bar<true>(bar(kBarXFree), (j & 1) ^ 1, abort_flag,
+                                                     p.status, kDevTimeoutXFree));
+        if (!ok) break;
+        const uint32_t rx = ptx::mapa(sX, peer) + t * (BN * 4);
+#pragma unroll
+        for (int q4 = 0; q4 < BN / 4; ++q4) {
+          const uint32_t off = ((q4 ^ (t & 15)) << 4);
+          ptx::st_cluster_v4(rx + off, __float_as_uint(s[4 * q4]), __float_as_uint(s[4 * q4 + 1]),
+                             __float_as_uint(s[4 * q4 + 2]), __float_as_uint(s[4 * q4 + 3]));
+        }
+        ptx::mbar_arrive_remote(ptx::mapa(bar(kBarXFull), peer));
+        ok = __all_sync(0xffffffffu, wait_bar<true>(bar(kBarXFull), j & 1, abort_flag, p.status,
+                                                     kDevTimeoutXFull));
+        if (!ok) break;
+        const uint32_t lx = sX + t * (BN * 4);
+#pragma unroll
+        for (int q4 = 0; q4 < BN / 4; ++q4) {
+          const uint32_t off = ((q4 ^ (t & 15)) << 4);
+          float a0, a1, a2, a3;
+          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
+                       : "r"(lx + off)
+                       : "memory");
+          s[4 * q4] += a0;
+          s[4 * q4 + 1] += a1;
+          s[4 * q4 + 2] += a2;
+          s[4 * q4 + 3] += a3;
+        }
+        ptx::mbar_arrive_remote(ptx::mapa(bar(kBarXFree), peer));
+      }
+
+      // Mask and row max.
+      const bool edge = (kb + BN > p.Lk) || (p.causal && kb + BN - 1 > w.pmin) ||
+                        (p.causal && p.window && kb < w.pmax - p.window + 1);
+      float mx = -INFINITY;
+      if (edge) {
+#pragma unroll
+        for (int e = 0; e < BN; ++e) {
+          const int kj = kb + e;
+          const bool vis = kj < p.Lk && (!p.causal || kj <= row_p) &&
+                           (!p.window || row_p - kj < p.window);
+          s[e] = vis ? s[e] : -INFINITY;
+          mx = fmaxf(mx, s[e]);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < BN; ++e) mx = fmaxf(mx, s[e]);
+      }
+      const float xm = (mx == -INFINITY) ? -INFINITY : mx * c;
+      const bool grow = xm > m_run + 8.0f;
+      const float m_old = m_run;
+      const bool rescale_o = grow && (m_old != -INFINITY) && (j > 0);
+      float alpha = 1.f;
+      if (grow) {
+        alpha = ptx::ex2(m_old - xm);  // 0 when m_old == -inf
+        l *= alpha;
+        m_run = xm;
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+
+      // Probabilities (log2 domain), row sum, pack to 16-bit pairs.
+      uint32_t pk[BN / 2];
+      float lsum = 0.f;
+#pragma unroll
+      for (int e = 0; e < BN; e += 2) {
+        float p0 = ptx::ex2(fmaf(s[e], c, -m_use));
+        float p1 = ptx::ex2(fmaf(s[e + 1], c, -m_use));
+        if (edge) {
+          p0 = (s[e] == -INFINITY) ? 0.f : p0;
+          p1 = (s[e + 1] == -INFINITY) ? 0.f : p1;
+        }
+        lsum += p0 + p1;
+        pk[e / 2] = pack2(p0, p1, BF16);
+      }
+      l += lsum;
+
+      // P buffer and O are free once the previous P.V product has completed.
+      if (j > 0) {
+        ok = __all_sync(0xffffffffu, wait_bar(bar(kBarPvDone), (j - 1) & 1, abort_flag,
+                                               p.status, kDevTimeoutPvDone));
+        if (!ok) break;
+        ptx::tc_fence_after();
+      }
+      if (__any_sync(0xffffffffu, rescale_o)) {
+        const float a = rescale_o ? alpha : 1.f;
+#pragma unroll 1
+        for (int cch = 0; cch < C::DH / 32; ++cch) {
+          uint32_t r[32];
+          ptx::tmem_ld32(lane_base + cch * 32, r);
+          ptx::tmem_wait_ld();
+          ptx::reg_fence(r);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * a);
+          ptx::tmem_st32(lane_base + cch * 32, r);
+        }
+        ptx::tmem_wait_st();
+      }
+      // P row -> shared memory, K-major 128B-swizzled (64 keys per 128-byte row).
+#pragma unroll
+      for (int ch = 0; ch < BN / 8; ++ch) {
+        const int blk = ch >> 3, cc = ch & 7;
+        const uint32_t addr = sP + blk * 16384 + t * 128 + ((cc ^ (t & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * ch]),
+                     "r"(pk[4 * ch + 1]), "r"(pk[4 * ch + 2]), "r"(pk[4 * ch + 3])
+                     : "memory");
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(kBarPFull));
+    }
+
+    if (ok && count > 0) {
+      ok = __all_sync(0xffffffffu, wait_bar(bar(kBarPvDone), (count - 1) & 1, abort_flag,
+                                             p.status, kDevTimeoutPvDone));
+      ptx::tc_fence_after();
+    }
+    // ---------------------------------------------------------------- epilogue
+    if (ok) {
+      if (p.write_partial) {
+        const long long R = static_cast<long long>(p.B) * p.Hq * p.Lq;
+        if (row_valid) {
+          const long long pr = static_cast<long long>(w.split) * R + row_id;
+          if (rank == 0) {
+            p.part_ml[2 * pr] = m_run;
+            p.part_ml[2 * pr + 1] = l;
+          }
+        }
+        if (count > 0) {
+#pragma unroll 1
+          for (int cch = 0; cch < C::DH / 32; ++cch) {
+            uint32_t r[32];
+            ptx::tmem_ld32(lane_base + cch * 32, r);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence(r);
+            if (row_valid) {
+              float4* dst = reinterpret_cast<float4*>(
+                  p.part_o + (static_cast<long long>(w.split) * R + row_id) * p.D + d0 + cch * 32);
+#pragma unroll
+              for (int q4 = 0; q4 < 8; ++q4)
+                dst[q4] = make_float4(__uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]),
+                                      __uint_as_float(r[4 * q4 + 2]),
+                                      __uint_as_float(r[4 * q4 + 3]));
+            }
+          }
+        }
+      } else if (count > 0) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+        for (int cch = 0; cch < C::DH / 32; ++cch) {
+          uint32_t r[32];
+          ptx::tmem_ld32(lane_base + cch * 32, r);
+          ptx::tmem_wait_ld();
+          ptx::reg_fence(r);
+          if (row_valid) {
+            uint4* dst = reinterpret_cast<uint4*>(p.out + row_id * p.D + d0 + cch * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint4 v;
+              v.x = pack2(__uint_as_float(r[8 * q4 + 0]) * inv, __uint_as_float(r[8 * q4 + 1]) * inv, BF16);
+              v.y = pack2(__uint_as_float(r[8 * q4 + 2]) * inv, __uint_as_float(r[8 * q4 + 3]) * inv, BF16);
+              v.z = pack2(__uint_as_float(r[8 * q4 + 4]) * inv, __uint_as_float(r[8 * q4 + 5]) * inv, BF16);
+              v.w = pack2(__uint_as_float(r[8 * q4 + 6]) * inv, __uint_as_float(r[8 * q4 + 7]) * inv, BF16);
+              dst[q4] = v;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // Let every copy and MMA this CTA started finish before its memory goes away.
+    if (warp == 4 && lane == 0) {
+      if (issued_q) wait_bar(bar(kBarQ), 0, abort_flag, p.status, kDevTimeoutDrain);
+      for (int s = 0; s < C::NSLOT; ++s)
+        if (static_cast<uint32_t>(s) < ring_issued) {
+          // the most recent load into slot s had sequence number `last`
+          const uint32_t last = s + ((ring_issued - 1 - s) / C::NSLOT) * C::NSLOT;
+          const uint32_t ph = (last / C::NSLOT) & 1;
+          const uint64_t t0 = ptx::globaltimer();
+          while (!ptx::mbar_try_wait(bar(kBarKvFull + s), ph) &&
+                 ptx::globaltimer() - t0 < kTimeoutNs) {
+          }
+        }
+    }
+    if (warp == 5 && lane == 0 && mma_issued) {
+      ptx::mma_commit(bar(kBarDrain));
+      const uint64_t t0 = ptx::globaltimer();
+      while (!ptx::mbar_try_wait(bar(kBarDrain), 0) && ptx::globaltimer() - t0 < kTimeoutNs) {
+      }
+    }
+    __syncthreads();
+  }
+  if (PAIR) ptx::cluster_sync();  // peer may still write into our X buffer until here
+  if (warp == 5) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+// Merge split partials: for each row, M = max_s m_s, l = sum_s 2^(m_s - M) l_s,
+// out = sum_s 2^(m_s - M) O_s / l, splits taken in increasing order, splits
+// that saw no visible key (l_s == 0) skipped.  One CTA per row; the maximum is
+// a warp-shuffle reduction, the weighted sums run in a fixed order, so a row's
+// result depends only on that row's partials.
+template <bool BF16>
+__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_o,
+                                                      const float* __restrict__ part_ml,
+                                                      uint16_t* __restrict__ out, long long R,
+                                                      int D, int n_splits) {
+  extern __shared__ float wts[];  // n_splits weights, then the total l
+  const long long row = blockIdx.x;
+  const int t = threadIdx.x;
+  if (t < 32) {
+    float mx = -INFINITY;
+    for (int s = t; s < n_splits; s += 32) {
+      const float ls = part_ml[2 * (s * R + row) + 1];
+      if (ls > 0.f) mx = fmaxf(mx, part_ml[2 * (s * R + row)]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    for (int s = t; s < n_splits; s += 32) {
+      const float ms = part_ml[2 * (s * R + row)];
+      const float ls = part_ml[2 * (s * R + row) + 1];
+      wts[s] = ls > 0.f ? ptx::ex2(ms - mx) : 0.f;
+    }
+  }
+  __syncthreads();
+  if (t == 0) {
+    float lt = 0.f;
+    for (int s = 0; s < n_splits; ++s)
+      if (wts[s] != 0.f) lt += wts[s] * part_ml[2 * (s * R + row) + 1];
+    wts[n_splits] = lt;
+  }
+  __syncthreads();
+  const float lt = wts[n_splits];
+  const float inv = lt > 0.f ? 1.f / lt : 0.f;
+  for (int d = 2 * t; d < D; d += 256) {
+    float a0 = 0.f, a1 = 0.f;
+    for (int s = 0; s < n_splits; ++s) {
+      const float ws = wts[s];
+      if (ws != 0.f) {
+        const float2 v = *reinterpret_cast<const float2*>(part_o + (s * R + row) * D + d);
+        a0 = fmaf(ws, v.x, a0);
+        a1 = fmaf(ws, v.y, a1);
+      }
+    }
+    *reinterpret_cast<uint32_t*>(out + row * D + d) = pack2(a0 * inv, a1 * inv, BF16);
+  }
+}
+
+}  // namespace gbsdpa

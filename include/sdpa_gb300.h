@@ -1,0 +1,139 @@
+/*
+ * sdpa_gb300.h -- C ABI of the fused scaled-dot-product attention library for
+ * NVIDIA GB300 (sm_103a), libsdpa_gb300.so.
+ *
+ * What every entry point computes
+ * --------------------------------
+ * For batch b, query head h and query row i:
+ *
+ *     G   = Hq / Hkv                 query heads per key/value head (GQA)
+ *     g   = h / G                    the key/value head that query head h reads
+ *     p_i = Lk - Lq + i              the row's position in the key sequence
+ *                                    (causal rows are aligned bottom-right)
+ *     visible keys j: (!causal || j <= p_i) && (window == 0 || p_i - j < window)
+ *     out[b,h,i,:] = sum_j softmax_j(scale * q[b,h,i,:] . k[b,g,j,:]) * v[b,g,j,:]
+ *
+ * with the softmax taken over the visible keys only.  This is the
+ * "matmul + softmax + matmul" attention of the page "fix: add head_dim=256 to
+ * fused SDPA full attention kernel" (MLX PR #3293, section "Benchmark: fused vs
+ * unfused SDPA for head_dim=256"), computed tile by tile so that the
+ * [heads, Lq, Lk] score matrix is never stored ("Fused SDPA full-attention for
+ * head_dim=192/256", MLX PR #3660, section "Microbenchmarks": the fused
+ * transient stays flat as kL grows).  Grouped-query heads follow the same page
+ * (n_q = 16 query heads over n_kv = 8 key/value heads); the causal flag and the
+ * sliding window follow "fix: gemma-4 long-prompt prefill OOMs on CUDA"
+ * (mlxcel issue #672, sections "Root cause" and "Suggested fix direction"),
+ * which replaces a dense [L, L] windowed mask by in-kernel masking; the window
+ * of 1024 and the bottom-right alignment of decode rows follow "fix: Gemma 4
+ * MTP never engages on CUDA (GB10)" (mlxcel issue #2160, sections "Current
+ * Behavior" and "Proposed Solution").
+ *
+ * Window convention: a window W keeps the W most recent keys including the
+ * row's own (p_i - j < W).  window == 0 means no window.
+ *
+ * Layout and ownership (all entry points)
+ * ---------------------------------------
+ *  q    [B, Hq,  Lq, D]  contiguous, fp16 or bf16, device memory
+ *  k    [B, Hkv, Lk, D]  contiguous, same dtype, device memory
+ *  v    [B, Hkv, Lk, D]  contiguous, same dtype, device memory
+ *  out  [B, Hq,  Lq, D]  contiguous, same dtype, device memory, written
+ *  Every pointer is owned by the caller, must be 16-byte aligned and must stay
+ *  valid until the work queued on `stream` has finished.  The library never
+ *  allocates device memory: where split partials are needed the caller passes
+ *  a workspace of at least the size the matching *_workspace_bytes call
+ *  returns (that size does not grow with Lk).
+ *  Supported: D in {256, 512}; dtype SDPA_F16 or SDPA_BF16.
+ *
+ * Errors
+ * ------
+ *  Calls are asynchronous on `stream`.  The return value reports argument
+ *  validation and launch errors only; on any non-zero return nothing has been
+ *  queued.  Device-side failures (a pipeline wait that gave up after 2 s) are
+ *  recorded in a per-device status word that sdpa_device_status() returns.
+ *  No entry point aborts the process.
+ */
+#ifndef SDPA_GB300_H_
+#define SDPA_GB300_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* sdpa_stream_t;
+
+enum sdpa_dtype { SDPA_F16 = 0, SDPA_BF16 = 1 };
+
+enum sdpa_status {
+  SDPA_OK = 0,
+  SDPA_ERR_INVALID_ARG = -1,    /* bad size, mask combination, NULL pointer, scale */
+  SDPA_ERR_UNSUPPORTED = -2,    /* head dim or dtype outside the supported set */
+  SDPA_ERR_WORKSPACE = -3,      /* workspace missing or smaller than required */
+  SDPA_ERR_CUDA = -4,           /* a CUDA runtime / driver call failed */
+  SDPA_ERR_DEVICE_TIMEOUT = -5, /* a kernel wait gave up (see sdpa_device_status) */
+  SDPA_ERR_ALIGNMENT = -6       /* a pointer is not 16-byte aligned */
+};
+
+/*
+ * Prefill / full attention: any Lq >= 1 (Lq <= Lk when causal).
+ *
+ * scale   multiplies q.k; must be finite and >= 0 (the pages use 1/sqrt(D)).
+ * causal  0 or 1; causal rows are aligned bottom-right (p_i = Lk - Lq + i).
+ * window  0 (none) or > 0 with causal = 1.
+ * workspace / workspace_bytes: optional.  With NULL (or too small a buffer) the
+ *   whole visible key range of each 128-row query tile is processed by one CTA;
+ *   with at least sdpa_prefill_workspace_bytes(...) bytes, long key ranges may
+ *   be split across CTAs and merged (fp32 partials), which keeps all SMs busy
+ *   when Lq is much smaller than Lk.
+ * Returns SDPA_OK or a negative sdpa_status.
+ */
+int sdpa_prefill(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
+                 int Lq, int Lk, int D, float scale, int causal, int window, int dtype,
+                 void* workspace, size_t workspace_bytes, sdpa_stream_t stream);
+
+/* Workspace that lets sdpa_prefill split long key ranges; 0 if it never would.
+ * Bounded by 8 * B * Hq * Lq * (D + 2) * 4 bytes, independent of Lk's size. */
+size_t sdpa_prefill_workspace_bytes(int B, int Hq, int Hkv, int Lq, int Lk, int D, int causal,
+                                    int window);
+
+/*
+ * Decode / speculative verify: 1 <= Lq <= 8 query rows per head over Lk keys.
+ *
+ * Same arguments and semantics as sdpa_prefill; the workspace is required
+ * (at least sdpa_decode_workspace_bytes(B, Hq, Hkv, Lq, D) bytes; the size
+ * does not depend on Lk).
+ *
+ * Row invariance ("fix: Gemma 4 MTP never engages on CUDA (GB10)", sections
+ * "Proposed Solution" and "Acceptance Criteria"): row i of a call with Lq = M
+ * is bit-identical to the Lq = 1 call with the same B, Hq, Hkv, D, dtype,
+ * scale, causal, window and workspace size whose key/value prefix is trimmed
+ * to Lk - M + 1 + i keys.  The key range is cut into 128-key tiles at fixed
+ * absolute positions, dealt round-robin over a split count that depends only
+ * on (B, Hkv, Hq/Hkv, D) and the device's SM count, and merged in a fixed
+ * order; a row's arithmetic never depends on the other rows of the call.
+ */
+int sdpa_decode(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
+                int Lq, int Lk, int D, float scale, int causal, int window, int dtype,
+                void* workspace, size_t workspace_bytes, sdpa_stream_t stream);
+
+/* Workspace bytes sdpa_decode needs on the current device (0 on bad arguments). */
+size_t sdpa_decode_workspace_bytes(int B, int Hq, int Hkv, int Lq, int D);
+
+/* Synchronises `stream`, returns SDPA_OK or SDPA_ERR_DEVICE_TIMEOUT for the
+ * current device and clears the status word.  *detail (if not NULL) receives
+ * the raw device code identifying the wait that gave up (0 if none). */
+int sdpa_device_status(sdpa_stream_t stream, int* detail);
+
+/* Human-readable text for an sdpa_status value (static storage). */
+const char* sdpa_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int sdpa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDPA_GB300_H_ */

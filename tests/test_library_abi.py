@@ -1,0 +1,88 @@
+"""The C-ABI library builds, loads and exports every entry point the header
+declares; host-side argument validation rejects bad calls before any CUDA call.
+
+No test here launches a kernel: they run on a machine without a GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import attention_sm_flash_attn_gb300 as gb
+from attention_sm_flash_attn_gb300 import build as gbbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "sdpa_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbbuild.build()
+    return gb.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(sdpa_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_expected_entry_points():
+    names = declared_functions()
+    assert set(gb.EXPORTED_SYMBOLS) == set(names), names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_version_and_status_strings(lib):
+    assert lib.sdpa_version() == 100
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert lib.sdpa_status_string(code).decode() != "unknown status"
+    assert lib.sdpa_status_string(-99).decode() == "unknown status"
+
+
+FAKE = ctypes.c_void_p(0x10000)   # a 16-byte aligned value; validation fails before any use
+ODD = ctypes.c_void_p(0x10008)
+
+
+def call(lib, fn, q=FAKE, k=FAKE, v=FAKE, out=FAKE, B=1, Hq=2, Hkv=1, Lq=4, Lk=8, D=256,
+         scale=0.0625, causal=1, window=0, dtype=0, ws=FAKE, ws_bytes=1 << 20):
+    return getattr(lib, fn)(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, dtype,
+                            ws, ws_bytes, None)
+
+
+BAD = [
+    (dict(q=None), -1), (dict(B=0), -1), (dict(Hq=3, Hkv=2), -1), (dict(Lk=0), -1),
+    (dict(causal=2), -1), (dict(window=-1), -1), (dict(causal=0, window=4), -1),
+    (dict(Lq=9, Lk=8), -1), (dict(scale=-1.0), -1), (dict(scale=float("nan")), -1),
+    (dict(D=128), -2), (dict(D=192), -2), (dict(dtype=2), -2), (dict(k=ODD), -6),
+]
+
+
+@pytest.mark.parametrize("fn", ["sdpa_prefill", "sdpa_decode"])
+@pytest.mark.parametrize("kw,code", BAD)
+def test_invalid_arguments_are_rejected_on_the_host(lib, fn, kw, code):
+    assert call(lib, fn, **kw) == code
+
+
+def test_decode_rejects_more_than_eight_rows(lib):
+    assert call(lib, "sdpa_decode", Lq=9, Lk=64) == -1
+
+
+def test_decode_requires_a_workspace(lib):
+    assert call(lib, "sdpa_decode", ws=None, ws_bytes=0) == -3
+
+
+def test_workspace_queries_reject_bad_shapes(lib):
+    assert lib.sdpa_decode_workspace_bytes(1, 3, 2, 1, 256) == 0
+    assert lib.sdpa_decode_workspace_bytes(1, 2, 1, 9, 256) == 0
+    assert lib.sdpa_prefill_workspace_bytes(1, 2, 1, 4, 8, 128, 1, 0) == 0
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError):
+        gb.load_library(str(tmp_path / "nope.so"))
