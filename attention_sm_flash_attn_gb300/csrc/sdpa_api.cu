@@ -118,7 +118,7 @@ int launch_attn(const AttnParams& p, long long items, cudaStream_t stream, Devic
   if (ctas <= 0 || ctas > 0x7fffffffll) return SDPA_ERR_INVALID_ARG;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
-  cfg.blockDim = dim3(192, 1, 1);
+  cfg.blockDim = dim3(Cfg<BF16, PAIR>::NTHREADS, 1, 1);
   cfg.dynamicSmemBytes = Cfg<BF16, PAIR>::SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -237,7 +237,9 @@ int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, i
   p.D = D;
   p.causal = causal;
   p.window = window;
-  p.c = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  // c = scale * log2(e), kept > 0 so that a masked score (-inf) maps to -inf;
+  // scale == 0 becomes a tiny c, for which every visible weight is exactly 1.
+  p.c = std::max(static_cast<float>(static_cast<double>(scale) * 1.4426950408889634), 1e-30f);
   p.decode = decode ? 1 : 0;
   p.n_qtiles = (Lq + 127) / 128;
   p.n_splits = n_splits;

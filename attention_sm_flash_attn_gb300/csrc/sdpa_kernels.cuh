@@ -58,6 +58,8 @@ enum : int {
   kDevTimeoutXFull = 0x107,
   kDevTimeoutXFree = 0x108,
   kDevTimeoutDrain = 0x109,
+  kDevTimeoutPair = 0x10a,
+  kDevMisaligned = 0x10b,
 };
 
 struct AttnParams {
@@ -84,6 +86,7 @@ struct Cfg {
   static constexpr int BM = 128;
   static constexpr int DH = 256;  // head-dim columns owned by one CTA
   static constexpr int BN = PAIR ? 64 : 128;
+  static constexpr int HB = BN / 2;  // key columns per softmax thread (two threads per row)
   static constexpr int NSLOT = PAIR ? 7 : 8;
   static constexpr int SLOT = 16384;
   static constexpr int KSUB = DH * BN * 2 / SLOT;   // K sub-tiles per key tile
@@ -96,8 +99,12 @@ struct Cfg {
   static constexpr int X_OFF = P_OFF + P_BYTES;
   static constexpr int X_BYTES = PAIR ? BM * BN * 4 : 0;
   static constexpr int BAR_OFF = X_OFF + X_BYTES;
-  static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
+  static constexpr int RED_OFF = BAR_OFF + 256;      // [2 parity][2 half][128 rows] floats
+  static constexpr int SMEM_BYTES = RED_OFF + 2048;
   static constexpr int S_COL = 256;  // TMEM: O in columns [0,256), S buffers after it
+  static constexpr int NTHREADS = 320;  // warps 0-7 softmax, 8 producer, 9 MMA
+  static constexpr int kProducerWarp = 8;
+  static constexpr int kMmaWarp = 9;
   static constexpr uint32_t IDESC_QK = ptx::idesc_f16(128, BN, BF16, false, false);
   static constexpr uint32_t IDESC_PV = ptx::idesc_f16(128, DH, BF16, false, true);
   static_assert(S_COL + 2 * BN <= 512, "TMEM budget");
@@ -116,7 +123,8 @@ enum {
   kBarXFull = 23,
   kBarXFree = 24,
   kBarDrain = 25,
-  kNumBars = 26,
+  kBarPair = 26,     // + lane quarter: row-max / row-sum exchange between the two halves
+  kNumBars = 30,
 };
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
@@ -211,21 +219,28 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
 }
 
 template <bool BF16, bool PAIR>
-__global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
   using C = Cfg<BF16, PAIR>;
   constexpr int BN = C::BN;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  constexpr int HB = C::HB;
+  extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = ptx::smem_u32(smem);
   const uint32_t sQ = sbase + C::Q_OFF;
   const uint32_t sRing = sbase + C::RING_OFF;
   const uint32_t sP = sbase + C::P_OFF;
   const uint32_t sX = sbase + C::X_OFF;
   const uint32_t sBar = sbase + C::BAR_OFF;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::BAR_OFF + 224);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 228);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::BAR_OFF + 240);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 244);
+  float* red = reinterpret_cast<float*>(smem + C::RED_OFF);
   auto bar = [&](int i) -> uint32_t { return sBar + 8u * static_cast<uint32_t>(i); };
+
+  // The swizzled tiles need a 1024-byte aligned base; the dynamic shared window
+  // provides it.  Should it ever not, fail cleanly instead of computing garbage.
+  if ((sbase & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicCAS(p.status, 0, kDevMisaligned);
+    return;
+  }
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -242,22 +257,23 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(bar(kBarSFull + b), 1);
-      ptx::mbar_init(bar(kBarSEmpty + b), 128);
+      ptx::mbar_init(bar(kBarSEmpty + b), 256);
     }
-    ptx::mbar_init(bar(kBarPFull), 128);
+    ptx::mbar_init(bar(kBarPFull), 256);
     ptx::mbar_init(bar(kBarPvDone), 1);
-    ptx::mbar_init(bar(kBarXFull), 128);
-    ptx::mbar_init(bar(kBarXFree), 128);
+    ptx::mbar_init(bar(kBarXFull), 256);
+    ptx::mbar_init(bar(kBarXFree), 256);
     ptx::mbar_init(bar(kBarDrain), 1);
+    for (int q = 0; q < 4; ++q) ptx::mbar_init(bar(kBarPair + q), 64);
     *abort_flag = 0;
     ptx::fence_mbarrier_init();
   }
-  if (warp == 4 && lane == 0 && !p.decode) {
+  if (warp == C::kProducerWarp && lane == 0 && !p.decode) {
     ptx::prefetch_tmap(&p.tm_q);
     ptx::prefetch_tmap(&p.tm_k);
     ptx::prefetch_tmap(&p.tm_v);
   }
-  if (warp == 5) {
+  if (warp == C::kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
     ptx::tmem_relinquish();
   }
@@ -273,7 +289,7 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
   uint32_t ring_issued = 0;  // ring loads issued, in sequence order
   int mma_issued = 0;
 
-  if (warp == 4) {
+  if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && count > 0) {
       const int bh_q = w.b * p.Hq + w.h0;
@@ -325,7 +341,7 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
       }
       if (ok) load_v(count - 1);
     }
-  } else if (warp == 5) {
+  } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && count > 0) {
       bool ok = wait_bar(bar(kBarQ), 0, abort_flag, p.status, kDevTimeoutQ);
@@ -408,9 +424,13 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
     }
   } else {
     // ------------------------------------------------------------ softmax / epilogue
-    const int t = threadIdx.x;  // row of the tile == TMEM lane
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    // Row identity.
+    // Two threads per row: warps q and q+4 read TMEM lanes [32q, 32q+32); `half`
+    // selects which half of the key columns (and of the O columns) a thread owns.
+    const int q4 = warp & 3;
+    const int half = warp >> 2;
+    const int t = q4 * 32 + lane;  // row of the tile == TMEM lane
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
+    const uint32_t pair_bar = bar(kBarPair + q4);
     int row_p;            // bottom-right position of this row
     bool row_valid;
     long long row_id;     // flat (b, h, i) row index, -1 if none
@@ -429,9 +449,10 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
       row_p = base + (row_valid ? i : 0);
       row_id = row_valid ? (static_cast<long long>(w.b) * p.Hq + h) * p.Lq + i : -1;
       if (count > 0) {
-        // Decode: stage this row's query slice into the swizzled Q tile.
+        // Decode: stage this thread's half of the row's query slice into the
+        // swizzled Q tile (16-byte chunks of 8 elements).
         const uint4* src = reinterpret_cast<const uint4*>(p.q + row_id * p.D + d0);
-        for (int c = 0; c < C::DH / 8; ++c) {  // 16-byte chunks of 8 elements
+        for (int c = half * (C::DH / 16); c < (half + 1) * (C::DH / 16); ++c) {
           uint4 v = make_uint4(0, 0, 0, 0);
           if (row_valid) v = src[c];
           const int dc = c >> 3, cc = c & 7;
@@ -441,35 +462,47 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
                        : "memory");
         }
         ptx::fence_proxy_async_smem();
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (t == 0) ptx::mbar_arrive(bar(kBarQ));
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (threadIdx.x == 0) ptx::mbar_arrive(bar(kBarQ));
       }
     }
 
     const float c = p.c;
-    float m_run = -INFINITY;  // running max of scale*log2e*s (lazy: may lag by < 8)
-    float l = 0.f;
+    float m_run = -INFINITY;  // running max of c * s (lazy: the true max may exceed it by < 8)
+    float l = 0.f;            // this half's share of the row sum
     bool ok = true;
     const uint32_t peer = rank ^ 1u;
+    int use = 0;  // pair-barrier uses so far
+
+    // Swap one float per row with the other half of the row (bounded wait).
+    auto swap_half = [&](float mine, float& other) -> bool {
+      float* slot = red + (use & 1) * 256;
+      slot[half * 128 + t] = mine;
+      ptx::mbar_arrive(pair_bar);
+      const bool got = __all_sync(0xffffffffu, wait_bar(pair_bar, use & 1, abort_flag, p.status,
+                                                         kDevTimeoutPair));
+      other = slot[(half ^ 1) * 128 + t];
+      ++use;
+      return got;
+    };
 
     for (int j = 0; j < count && ok; ++j) {
       const int tile = w.t_begin + j * w.t_step;
-      const int kb = tile * BN;
+      const int kb = tile * BN + half * HB;  // first key of this thread's columns
       const int buf = j & 1;
-      ok = __all_sync(0xffffffffu,
-                      wait_bar(bar(kBarSFull + buf), (j >> 1) & 1, abort_flag, p.status,
-                               kDevTimeoutSFull));
+      ok = __all_sync(0xffffffffu, wait_bar(bar(kBarSFull + buf), (j >> 1) & 1, abort_flag,
+                                             p.status, kDevTimeoutSFull));
       if (!ok) break;
       ptx::tc_fence_after();
-      float s[BN];
+      float s[HB];
       {
-        uint32_t r[BN / 32][32];
+        uint32_t r[HB / 32][32];
 #pragma unroll
-        for (int cch = 0; cch < BN / 32; ++cch)
-          ptx::tmem_ld32(lane_base + C::S_COL + buf * BN + cch * 32, r[cch]);
+        for (int cch = 0; cch < HB / 32; ++cch)
+          ptx::tmem_ld32(lane_base + C::S_COL + buf * BN + half * HB + cch * 32, r[cch]);
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int cch = 0; cch < BN / 32; ++cch) {
+        for (int cch = 0; cch < HB / 32; ++cch) {
           ptx::reg_fence(r[cch]);
 #pragma unroll
           for (int e = 0; e < 32; ++e) s[cch * 32 + e] = __uint_as_float(r[cch][e]);
@@ -479,16 +512,17 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
       ptx::mbar_arrive(bar(kBarSEmpty + buf));
 
       if constexpr (PAIR) {
-        // Swap partial scores with the peer CTA and add them.
+        // Swap partial scores with the peer CTA (same columns) and add them.
         ok = __all_sync(0xffffffffu, wait_bar<true>(bar(kBarXFree), (j & 1) ^ 1, abort_flag,
                                                      p.status, kDevTimeoutXFree));
         if (!ok) break;
         const uint32_t rx = ptx::mapa(sX, peer) + t * (BN * 4);
 #pragma unroll
-        for (int q4 = 0; q4 < BN / 4; ++q4) {
-          const uint32_t off = ((q4 ^ (t & 15)) << 4);
-          ptx::st_cluster_v4(rx + off, __float_as_uint(s[4 * q4]), __float_as_uint(s[4 * q4 + 1]),
-                             __float_as_uint(s[4 * q4 + 2]), __float_as_uint(s[4 * q4 + 3]));
+        for (int g = 0; g < HB / 4; ++g) {
+          const int gq = half * (HB / 4) + g;
+          const uint32_t off = ((gq ^ (t & 15)) << 4);
+          ptx::st_cluster_v4(rx + off, __float_as_uint(s[4 * g]), __float_as_uint(s[4 * g + 1]),
+                             __float_as_uint(s[4 * g + 2]), __float_as_uint(s[4 * g + 3]));
         }
         ptx::mbar_arrive_remote(ptx::mapa(bar(kBarXFull), peer));
         ok = __all_sync(0xffffffffu, wait_bar<true>(bar(kBarXFull), j & 1, abort_flag, p.status,
@@ -496,39 +530,52 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
         if (!ok) break;
         const uint32_t lx = sX + t * (BN * 4);
 #pragma unroll
-        for (int q4 = 0; q4 < BN / 4; ++q4) {
-          const uint32_t off = ((q4 ^ (t & 15)) << 4);
+        for (int g = 0; g < HB / 4; ++g) {
+          const int gq = half * (HB / 4) + g;
+          const uint32_t off = ((gq ^ (t & 15)) << 4);
           float a0, a1, a2, a3;
           asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                        : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
                        : "r"(lx + off)
                        : "memory");
-          s[4 * q4] += a0;
-          s[4 * q4 + 1] += a1;
-          s[4 * q4 + 2] += a2;
-          s[4 * q4 + 3] += a3;
+          // rank 0 adds (own + peer), rank 1 adds (peer + own): the same two
+          // operands, so both CTAs hold bit-identical scores.
+          s[4 * g] += a0;
+          s[4 * g + 1] += a1;
+          s[4 * g + 2] += a2;
+          s[4 * g + 3] += a3;
         }
         ptx::mbar_arrive_remote(ptx::mapa(bar(kBarXFree), peer));
       }
 
-      // Mask and row max.
-      const bool edge = (kb + BN > p.Lk) || (p.causal && kb + BN - 1 > w.pmin) ||
-                        (p.causal && p.window && kb < w.pmax - p.window + 1);
-      float mx = -INFINITY;
+      // Mask (only on tiles that straddle the band edge or the end of the keys).
+      const int tb = tile * BN;
+      const bool edge = (tb + BN > p.Lk) || (p.causal && tb + BN - 1 > w.pmin) ||
+                        (p.causal && p.window && tb < w.pmax - p.window + 1);
       if (edge) {
 #pragma unroll
-        for (int e = 0; e < BN; ++e) {
+        for (int e = 0; e < HB; ++e) {
           const int kj = kb + e;
           const bool vis = kj < p.Lk && (!p.causal || kj <= row_p) &&
                            (!p.window || row_p - kj < p.window);
           s[e] = vis ? s[e] : -INFINITY;
-          mx = fmaxf(mx, s[e]);
         }
-      } else {
-#pragma unroll
-        for (int e = 0; e < BN; ++e) mx = fmaxf(mx, s[e]);
       }
-      const float xm = (mx == -INFINITY) ? -INFINITY : mx * c;
+      // Row max: tree over this half, then swap with the other half.
+      float mh;
+      {
+        float mm[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mm[k] = s[k];
+#pragma unroll
+        for (int e = 8; e < HB; ++e) mm[e & 7] = fmaxf(mm[e & 7], s[e]);
+        mh = fmaxf(fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3])),
+                   fmaxf(fmaxf(mm[4], mm[5]), fmaxf(mm[6], mm[7])));
+      }
+      float mo;
+      ok = swap_half(mh, mo);
+      if (!ok) break;
+      const float xm = fmaxf(mh, mo) * c;  // c > 0, so -inf stays -inf
       const bool grow = xm > m_run + 8.0f;
       const float m_old = m_run;
       const bool rescale_o = grow && (m_old != -INFINITY) && (j > 0);
@@ -540,23 +587,21 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
 
-      // Probabilities (log2 domain), row sum, pack to 16-bit pairs.
-      uint32_t pk[BN / 2];
-      float lsum = 0.f;
+      // Probabilities 2^(c*s - m), partial row sum, pack to 16-bit pairs.
+      uint32_t pk[HB / 2];
+      float ls[8];
 #pragma unroll
-      for (int e = 0; e < BN; e += 2) {
-        float p0 = ptx::ex2(fmaf(s[e], c, -m_use));
-        float p1 = ptx::ex2(fmaf(s[e + 1], c, -m_use));
-        if (edge) {
-          p0 = (s[e] == -INFINITY) ? 0.f : p0;
-          p1 = (s[e + 1] == -INFINITY) ? 0.f : p1;
-        }
-        lsum += p0 + p1;
+      for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+#pragma unroll
+      for (int e = 0; e < HB; e += 2) {
+        const float p0 = ptx::ex2(fmaf(s[e], c, -m_use));
+        const float p1 = ptx::ex2(fmaf(s[e + 1], c, -m_use));
+        ls[(e >> 1) & 7] += p0 + p1;
         pk[e / 2] = pack2(p0, p1, BF16);
       }
-      l += lsum;
+      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
 
-      // P buffer and O are free once the previous P.V product has completed.
+      // The P buffer and O are free once the previous P.V product has completed.
       if (j > 0) {
         ok = __all_sync(0xffffffffu, wait_bar(bar(kBarPvDone), (j - 1) & 1, abort_flag,
                                                p.status, kDevTimeoutPvDone));
@@ -566,21 +611,23 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
       if (__any_sync(0xffffffffu, rescale_o)) {
         const float a = rescale_o ? alpha : 1.f;
 #pragma unroll 1
-        for (int cch = 0; cch < C::DH / 32; ++cch) {
+        for (int cch = 0; cch < C::DH / 64; ++cch) {
+          const uint32_t col = half * (C::DH / 2) + cch * 32;
           uint32_t r[32];
-          ptx::tmem_ld32(lane_base + cch * 32, r);
+          ptx::tmem_ld32(lane_base + col, r);
           ptx::tmem_wait_ld();
           ptx::reg_fence(r);
 #pragma unroll
           for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * a);
-          ptx::tmem_st32(lane_base + cch * 32, r);
+          ptx::tmem_st32(lane_base + col, r);
         }
         ptx::tmem_wait_st();
       }
       // P row -> shared memory, K-major 128B-swizzled (64 keys per 128-byte row).
 #pragma unroll
-      for (int ch = 0; ch < BN / 8; ++ch) {
-        const int blk = ch >> 3, cc = ch & 7;
+      for (int ch = 0; ch < HB / 8; ++ch) {
+        const int gc = half * (HB / 8) + ch;
+        const int blk = gc >> 3, cc = gc & 7;
         const uint32_t addr = sP + blk * 16384 + t * 128 + ((cc ^ (t & 7)) << 4);
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * ch]),
                      "r"(pk[4 * ch + 1]), "r"(pk[4 * ch + 2]), "r"(pk[4 * ch + 3])
@@ -595,54 +642,56 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
       ok = __all_sync(0xffffffffu, wait_bar(bar(kBarPvDone), (count - 1) & 1, abort_flag,
                                              p.status, kDevTimeoutPvDone));
       ptx::tc_fence_after();
+      float lo = 0.f;
+      if (ok) ok = swap_half(l, lo);
+      l = half == 0 ? l + lo : lo + l;  // both halves: l_0 + l_1
     }
     // ---------------------------------------------------------------- epilogue
     if (ok) {
       if (p.write_partial) {
         const long long R = static_cast<long long>(p.B) * p.Hq * p.Lq;
-        if (row_valid) {
+        if (row_valid && half == 0 && rank == 0) {
           const long long pr = static_cast<long long>(w.split) * R + row_id;
-          if (rank == 0) {
-            p.part_ml[2 * pr] = m_run;
-            p.part_ml[2 * pr + 1] = l;
-          }
+          p.part_ml[2 * pr] = m_run;
+          p.part_ml[2 * pr + 1] = l;
         }
         if (count > 0) {
 #pragma unroll 1
-          for (int cch = 0; cch < C::DH / 32; ++cch) {
+          for (int cch = 0; cch < C::DH / 64; ++cch) {
+            const int col = half * (C::DH / 2) + cch * 32;
             uint32_t r[32];
-            ptx::tmem_ld32(lane_base + cch * 32, r);
+            ptx::tmem_ld32(lane_base + col, r);
             ptx::tmem_wait_ld();
             ptx::reg_fence(r);
             if (row_valid) {
               float4* dst = reinterpret_cast<float4*>(
-                  p.part_o + (static_cast<long long>(w.split) * R + row_id) * p.D + d0 + cch * 32);
+                  p.part_o + (static_cast<long long>(w.split) * R + row_id) * p.D + d0 + col);
 #pragma unroll
-              for (int q4 = 0; q4 < 8; ++q4)
-                dst[q4] = make_float4(__uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]),
-                                      __uint_as_float(r[4 * q4 + 2]),
-                                      __uint_as_float(r[4 * q4 + 3]));
+              for (int g = 0; g < 8; ++g)
+                dst[g] = make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                                     __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
             }
           }
         }
       } else if (count > 0) {
         const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-        for (int cch = 0; cch < C::DH / 32; ++cch) {
+        for (int cch = 0; cch < C::DH / 64; ++cch) {
+          const int col = half * (C::DH / 2) + cch * 32;
           uint32_t r[32];
-          ptx::tmem_ld32(lane_base + cch * 32, r);
+          ptx::tmem_ld32(lane_base + col, r);
           ptx::tmem_wait_ld();
           ptx::reg_fence(r);
           if (row_valid) {
-            uint4* dst = reinterpret_cast<uint4*>(p.out + row_id * p.D + d0 + cch * 32);
+            uint4* dst = reinterpret_cast<uint4*>(p.out + row_id * p.D + d0 + col);
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+            for (int g = 0; g < 4; ++g) {
               uint4 v;
-              v.x = pack2(__uint_as_float(r[8 * q4 + 0]) * inv, __uint_as_float(r[8 * q4 + 1]) * inv, BF16);
-              v.y = pack2(__uint_as_float(r[8 * q4 + 2]) * inv, __uint_as_float(r[8 * q4 + 3]) * inv, BF16);
-              v.z = pack2(__uint_as_float(r[8 * q4 + 4]) * inv, __uint_as_float(r[8 * q4 + 5]) * inv, BF16);
-              v.w = pack2(__uint_as_float(r[8 * q4 + 6]) * inv, __uint_as_float(r[8 * q4 + 7]) * inv, BF16);
-              dst[q4] = v;
+              v.x = pack2(__uint_as_float(r[8 * g + 0]) * inv, __uint_as_float(r[8 * g + 1]) * inv, BF16);
+              v.y = pack2(__uint_as_float(r[8 * g + 2]) * inv, __uint_as_float(r[8 * g + 3]) * inv, BF16);
+              v.z = pack2(__uint_as_float(r[8 * g + 4]) * inv, __uint_as_float(r[8 * g + 5]) * inv, BF16);
+              v.w = pack2(__uint_as_float(r[8 * g + 6]) * inv, __uint_as_float(r[8 * g + 7]) * inv, BF16);
+              dst[g] = v;
             }
           }
         }
@@ -655,7 +704,7 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
   __syncthreads();
   if (*abort_flag) {
     // Let every copy and MMA this CTA started finish before its memory goes away.
-    if (warp == 4 && lane == 0) {
+    if (warp == C::kProducerWarp && lane == 0) {
       if (issued_q) wait_bar(bar(kBarQ), 0, abort_flag, p.status, kDevTimeoutDrain);
       for (int s = 0; s < C::NSLOT; ++s)
         if (static_cast<uint32_t>(s) < ring_issued) {
@@ -668,7 +717,7 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
           }
         }
     }
-    if (warp == 5 && lane == 0 && mma_issued) {
+    if (warp == C::kMmaWarp && lane == 0 && mma_issued) {
       ptx::mma_commit(bar(kBarDrain));
       const uint64_t t0 = ptx::globaltimer();
       while (!ptx::mbar_try_wait(bar(kBarDrain), 0) && ptx::globaltimer() - t0 < kTimeoutNs) {
@@ -677,7 +726,7 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_kernel(const __grid_constant_
     __syncthreads();
   }
   if (PAIR) ptx::cluster_sync();  // peer may still write into our X buffer until here
-  if (warp == 5) {
+  if (warp == C::kMmaWarp) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
   }
