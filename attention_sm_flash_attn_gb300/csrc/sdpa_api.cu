@@ -353,6 +353,8 @@ const char* sdpa_status_string(int status) {
     case SDPA_ERR_CUDA: return "CUDA runtime or driver call failed";
     case SDPA_ERR_DEVICE_TIMEOUT: return "a kernel wait gave up (device timeout)";
     case SDPA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case SDPA_ERR_SCRATCH_LIMIT:
+      return "call needs more than the built-in scratch of sdpa_decode_noalloc";
     default: return "unknown status";
   }
 }
@@ -360,3 +362,55 @@ const char* sdpa_status_string(int status) {
 int sdpa_version(void) { return 100; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode: the split partials go to a scratch array that is part
+// of the library image instead of a caller workspace.
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SDPA_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once per
+// device.  The array's name is only a host-side handle; the kernels must be
+// given this address.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SDPA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
+      return SDPA_ERR_CUDA;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return SDPA_OK;
+}
+
+}  // namespace
+
+extern "C" int sdpa_decode_noalloc(const void* q, const void* k, const void* v, void* out, int B,
+                                   int Hq, int Hkv, int Lq, int Lk, int D, float scale,
+                                   int causal, int window, int dtype, sdpa_stream_t stream) {
+  int rc = validate(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, dtype);
+  if (rc) return rc;
+  if (Lq > 8) return SDPA_ERR_INVALID_ARG;
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc) return rc;
+  const int s = plan_decode_splits(st->sms, B, Hq, Hkv, D);
+  if (partial_bytes(static_cast<long long>(B) * Hq * Lq, D, s) > SDPA_NOALLOC_SCRATCH_BYTES)
+    return SDPA_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  rc = noalloc_scratch(&scratch);
+  if (rc) return rc;
+  auto strm = reinterpret_cast<cudaStream_t>(stream);
+  return dtype == SDPA_BF16
+             ? run<true>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, true, s,
+                         true, scratch, strm, st)
+             : run<false>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, true, s,
+                          true, scratch, strm, st);
+}

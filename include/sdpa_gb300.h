@@ -73,7 +73,9 @@ enum sdpa_status {
   SDPA_ERR_WORKSPACE = -3,      /* workspace missing or smaller than required */
   SDPA_ERR_CUDA = -4,           /* a CUDA runtime / driver call failed */
   SDPA_ERR_DEVICE_TIMEOUT = -5, /* a kernel wait gave up (see sdpa_device_status) */
-  SDPA_ERR_ALIGNMENT = -6       /* a pointer is not 16-byte aligned */
+  SDPA_ERR_ALIGNMENT = -6,      /* a pointer is not 16-byte aligned */
+  SDPA_ERR_SCRATCH_LIMIT = -7   /* sdpa_decode_noalloc: the call needs more than its built-in
+                                   scratch (SDPA_NOALLOC_SCRATCH_BYTES) */
 };
 
 /*
@@ -131,6 +133,41 @@ const char* sdpa_status_string(int status);
 
 /* Library ABI version (major * 100 + minor). */
 int sdpa_version(void);
+
+/*
+ * sdpa_decode_noalloc -- sdpa_decode for callers that cannot allocate device
+ * memory.  (The paper, i.e. the web pages this library follows, has no
+ * counterpart of this entry point; it is a convenience of this library.)
+ *
+ * Who needs it: code that runs inside a host runtime which owns the device
+ * heap and forbids allocation on its execution path (for example a plugin
+ * whose enqueue callback may only launch work), and latency-critical loops
+ * where a cudaMalloc, with the device-wide synchronisation it can imply, is
+ * not acceptable.  Such callers cannot hand sdpa_decode a workspace.
+ *
+ * Instead of a caller workspace this entry point uses a scratch array of
+ * SDPA_NOALLOC_SCRATCH_BYTES that lives in the library itself (a static
+ * __device__ array: every GPU that loads the library holds it until the
+ * process exits).  It calls no cudaMalloc, cudaFree or other allocating
+ * routine.  The caller still provides q, k, v and out exactly as for
+ * sdpa_decode, and the results are those of sdpa_decode.
+ *
+ *  - The first call on each device looks up the device address of the scratch
+ *    array (cudaGetSymbolAddress with that device current); make that first
+ *    call before any stream capture on that device.
+ *  - A call whose split partials need more than SDPA_NOALLOC_SCRATCH_BYTES is
+ *    rejected with SDPA_ERR_SCRATCH_LIMIT before anything is queued; the need
+ *    is what sdpa_decode_workspace_bytes(B, Hq, Hkv, Lq, D) reports.
+ *  - Every call on a device shares the one array, and the array keeps the
+ *    previous call's contents.  Nothing in it has to start at zero: each call
+ *    writes every partial it later reads.  Two calls whose work overlaps on
+ *    the GPU (different streams, no ordering between them) race on the array
+ *    and give wrong results: serialise them, e.g. on one stream.
+ */
+#define SDPA_NOALLOC_SCRATCH_BYTES ((size_t)24 << 20)
+int sdpa_decode_noalloc(const void* q, const void* k, const void* v, void* out, int B, int Hq,
+                        int Hkv, int Lq, int Lk, int D, float scale, int causal, int window,
+                        int dtype, sdpa_stream_t stream);
 
 #ifdef __cplusplus
 }
