@@ -27,7 +27,7 @@ struct DeviceState {
   bool ready = false;
   int sms = 0;
   int* status = nullptr;  // device address of g_device_status
-  bool attr_set[4] = {false, false, false, false};
+  bool attr_set[6] = {false, false, false, false, false, false};
 };
 
 std::mutex g_mu;
@@ -98,31 +98,32 @@ int validate(const void* q, const void* k, const void* v, const void* out, int B
   return SDPA_OK;
 }
 
-template <bool BF16, bool PAIR>
+template <bool BF16, int MODE>
 int ensure_attr(DeviceState* st) {
-  const int idx = (BF16 ? 1 : 0) + (PAIR ? 2 : 0);
+  const int idx = (BF16 ? 1 : 0) + 2 * MODE;
   if (st->attr_set[idx]) return SDPA_OK;
-  auto kern = gbsdpa::attn_fwd_kernel<BF16, PAIR>;
+  auto kern = gbsdpa::attn_fwd_kernel<BF16, MODE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg<BF16, PAIR>::SMEM_BYTES) != cudaSuccess)
+                           Cfg<BF16, MODE>::SMEM_BYTES) != cudaSuccess)
     return SDPA_ERR_CUDA;
   st->attr_set[idx] = true;
   return SDPA_OK;
 }
 
-template <bool BF16, bool PAIR>
+template <bool BF16, int MODE>
 int launch_attn(const AttnParams& p, long long items, cudaStream_t stream, DeviceState* st) {
-  int rc = ensure_attr<BF16, PAIR>(st);
+  int rc = ensure_attr<BF16, MODE>(st);
   if (rc) return rc;
-  const long long ctas = items * (PAIR ? 2 : 1);
+  constexpr bool kCluster = MODE != gbsdpa::kSingle;
+  const long long ctas = items * (kCluster ? 2 : 1);
   if (ctas <= 0 || ctas > 0x7fffffffll) return SDPA_ERR_INVALID_ARG;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
-  cfg.blockDim = dim3(Cfg<BF16, PAIR>::NTHREADS, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<BF16, PAIR>::SMEM_BYTES;
+  cfg.blockDim = dim3(Cfg<BF16, MODE>::NTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<BF16, MODE>::SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  if (PAIR) {
+  if (kCluster) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
@@ -130,19 +131,21 @@ int launch_attn(const AttnParams& p, long long items, cudaStream_t stream, Devic
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gbsdpa::attn_fwd_kernel<BF16, PAIR>, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gbsdpa::attn_fwd_kernel<BF16, MODE>, p);
   return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
 int launch_combine(const float* part_o, const float* part_ml, void* out, long long R, int D,
                    int n_splits, bool bf16, cudaStream_t stream) {
-  const size_t sh = static_cast<size_t>(n_splits + 1) * sizeof(float);
-  if (R <= 0 || R > 0x7fffffffll) return SDPA_ERR_INVALID_ARG;
+  // weights (n_splits + 1, padded to 4 floats) then 8 x 32 float4 warp sums
+  const size_t sh = static_cast<size_t>((n_splits + 4) & ~3) * sizeof(float) + 8 * 32 * 16;
+  if (R <= 0 || R > 0x7fffffffll || D % 128 != 0) return SDPA_ERR_INVALID_ARG;
+  const dim3 grid(static_cast<unsigned>(R), static_cast<unsigned>(D / 128));
   if (bf16)
-    gbsdpa::combine_kernel<true><<<static_cast<unsigned>(R), 128, sh, stream>>>(
+    gbsdpa::combine_kernel<true><<<grid, gbsdpa::kCombineThreads, sh, stream>>>(
         part_o, part_ml, static_cast<uint16_t*>(out), R, D, n_splits);
   else
-    gbsdpa::combine_kernel<false><<<static_cast<unsigned>(R), 128, sh, stream>>>(
+    gbsdpa::combine_kernel<false><<<grid, gbsdpa::kCombineThreads, sh, stream>>>(
         part_o, part_ml, static_cast<uint16_t*>(out), R, D, n_splits);
   return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
@@ -154,14 +157,24 @@ size_t partial_bytes(long long R, int D, int n_splits) {
   return ((po + 255) & ~static_cast<size_t>(255)) + ((pm + 255) & ~static_cast<size_t>(255));
 }
 
-// Key tiles (of `bn` keys) the longest 128-row query tile visits.
-long long max_tiles_per_qtile(int Lq, int Lk, int causal, int window, int bn) {
-  const int m0 = ((Lq - 1) / 128) * 128;  // last query tile sees the most keys when causal
-  const int pmin = Lk - Lq + m0, pmax = Lk - 1;
-  const int lo = (causal && window) ? std::max(0, pmin - window + 1) : 0;
-  const int hi = causal ? std::min(Lk, pmax + 1) : Lk;
+// Kernel variant for a call: head_dim 512 splits the head dimension over a CTA
+// pair; head_dim 256 prefill uses 2-SM MMAs over 256-row query tiles; decode
+// uses one CTA per 16 query heads x 8 position slots.
+int choose_mode(bool decode, int D) {
+  if (D == 512) return gbsdpa::kPair;
+  return decode ? gbsdpa::kSingle : gbsdpa::kDuo;
+}
+
+int qtile_rows(int mode) { return mode == gbsdpa::kDuo ? 256 : 128; }
+int key_tile(int mode) { return mode == gbsdpa::kPair ? 64 : 128; }
+
+// Key tiles the longest query tile (of `rows` rows) visits.
+long long max_tiles_per_qtile(int Lq, int Lk, int causal, int window, int bn, int rows) {
   if (!causal) return (Lk + bn - 1) / bn;
-  (void)pmin;
+  const int q0 = ((Lq - 1) / rows) * rows;  // the last query tile sees the most keys
+  const int pmin = Lk - Lq + q0, pmax = Lk - 1;
+  const int lo = window ? std::max(0, pmin - window + 1) : 0;
+  const int hi = std::min(Lk, pmax + 1);
   return (hi + bn - 1) / bn - lo / bn;
 }
 
@@ -169,12 +182,12 @@ long long max_tiles_per_qtile(int Lq, int Lk, int causal, int window, int bn) {
 // simple wave model: time ~ ceil(ctas / sms) * ceil(tiles / s), plus the cost
 // of writing and re-reading the fp32 partials.
 int plan_prefill_splits(int sms, int B, int Hq, int Lq, int Lk, int D, int causal, int window) {
-  const bool pair = D == 512;
-  const int bn = pair ? 64 : 128;
-  const long long items = static_cast<long long>(B) * Hq * ((Lq + 127) / 128);
-  const long long per_cta = pair ? 2 : 1;
+  const int mode = choose_mode(false, D);
+  const int bn = key_tile(mode), rows = qtile_rows(mode);
+  const long long items = static_cast<long long>(B) * Hq * ((Lq + rows - 1) / rows);
+  const long long per_cta = mode == gbsdpa::kSingle ? 1 : 2;
   const long long slots = std::max<long long>(1, sms / per_cta);
-  const long long T = max_tiles_per_qtile(Lq, Lk, causal, window, bn);
+  const long long T = max_tiles_per_qtile(Lq, Lk, causal, window, bn, rows);
   if (items >= 2 * slots || T < 16) return 1;
   // one key tile ~ 4 * 128 * bn * 256 flop per CTA at ~8 Kflop/clk, ~1.9 GHz
   const double t_tile_us = 4.0 * 128 * bn * 256 / 8192.0 / 1900.0;
@@ -209,14 +222,17 @@ int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, i
         bool write_partial, void* workspace, cudaStream_t stream, DeviceState* st) {
   AttnParams p;
   std::memset(&p, 0, sizeof(p));
-  const bool pair = D == 512;
-  const int bn = pair ? 64 : 128;
+  const int mode = choose_mode(decode, D);
+  // K boxes: all keys of a tile (one CTA), or the CTA's 64 keys (pair kernels);
+  // V boxes: 32 keys (one CTA, head-dim split) or 64 keys (2-SM MMA).
+  const int k_rows = mode == gbsdpa::kSingle ? 128 : 64;
+  const int v_rows = mode == gbsdpa::kDuo ? 64 : 32;
   int rc = SDPA_OK;
   if (!decode) rc = encode_map(&p.tm_q, q, D, Lq, static_cast<long long>(B) * Hq, 128, BF16);
   if (rc) return rc;
-  rc = encode_map(&p.tm_k, k, D, Lk, static_cast<long long>(B) * Hkv, bn, BF16);
+  rc = encode_map(&p.tm_k, k, D, Lk, static_cast<long long>(B) * Hkv, k_rows, BF16);
   if (rc) return rc;
-  rc = encode_map(&p.tm_v, v, D, Lk, static_cast<long long>(B) * Hkv, 32, BF16);
+  rc = encode_map(&p.tm_v, v, D, Lk, static_cast<long long>(B) * Hkv, v_rows, BF16);
   if (rc) return rc;
   const long long R = static_cast<long long>(B) * Hq * Lq;
   p.q = static_cast<const uint16_t*>(q);
@@ -241,7 +257,7 @@ int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, i
   // scale == 0 becomes a tiny c, for which every visible weight is exactly 1.
   p.c = std::max(static_cast<float>(static_cast<double>(scale) * 1.4426950408889634), 1e-30f);
   p.decode = decode ? 1 : 0;
-  p.n_qtiles = (Lq + 127) / 128;
+  p.n_qtiles = (Lq + qtile_rows(mode) - 1) / qtile_rows(mode);
   p.n_splits = n_splits;
   p.n_hb = (p.G + 15) / 16;
   p.write_partial = write_partial ? 1 : 0;
@@ -250,8 +266,11 @@ int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, i
     items = static_cast<long long>(B) * Hkv * n_splits * p.n_hb;
   else
     items = static_cast<long long>(B) * Hq * p.n_qtiles * n_splits;
-  rc = pair ? launch_attn<BF16, true>(p, items, stream, st)
-            : launch_attn<BF16, false>(p, items, stream, st);
+  switch (mode) {
+    case gbsdpa::kPair: rc = launch_attn<BF16, gbsdpa::kPair>(p, items, stream, st); break;
+    case gbsdpa::kDuo: rc = launch_attn<BF16, gbsdpa::kDuo>(p, items, stream, st); break;
+    default: rc = launch_attn<BF16, gbsdpa::kSingle>(p, items, stream, st); break;
+  }
   if (rc) return rc;
   if (write_partial)
     rc = launch_combine(p.part_o, p.part_ml, out, R, D, n_splits, BF16, stream);

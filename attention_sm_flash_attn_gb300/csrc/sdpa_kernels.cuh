@@ -58,7 +58,7 @@ enum : int {
   kDevTimeoutXFull = 0x107,
   kDevTimeoutXFree = 0x108,
   kDevTimeoutDrain = 0x109,
-  kDevTimeoutPair = 0x10a,
+  kDevTimeoutPair = 0x10a,  // (unused: the row halves now meet at a named barrier)
   kDevMisaligned = 0x10b,
 };
 
@@ -81,34 +81,56 @@ struct AttnParams {
   int write_partial;
 };
 
-template <bool BF16, bool PAIR>
+// Kernel variants.
+//   kSingle: one CTA per 128 query rows, head_dim 256 (decode, and prefill fallback).
+//   kPair:   head_dim 512; a 2-CTA cluster splits the head dimension and swaps
+//            partial scores through distributed shared memory.
+//   kDuo:    head_dim 256 prefill with 2-SM MMAs (cta_group::2): a 2-CTA
+//            cluster owns 256 query rows; each CTA loads half of every K and V
+//            tile, which halves the bytes each SM stages per FLOP.
+enum Mode : int { kSingle = 0, kPair = 1, kDuo = 2 };
+
+template <bool BF16, int MODE>
 struct Cfg {
-  static constexpr int BM = 128;
-  static constexpr int DH = 256;  // head-dim columns owned by one CTA
-  static constexpr int BN = PAIR ? 64 : 128;
-  static constexpr int HB = BN / 2;  // key columns per softmax thread (two threads per row)
-  static constexpr int NSLOT = PAIR ? 7 : 8;
+  static constexpr bool PAIR = MODE == kPair;
+  static constexpr bool DUO = MODE == kDuo;
+  static constexpr int BM = 128;                   // query rows per CTA
+  static constexpr int DH = 256;                   // head-dim columns owned by one CTA
+  static constexpr int BN = PAIR ? 64 : 128;       // keys per tile
+  static constexpr int HB = BN / 2;                // key columns per softmax thread
+  static constexpr int NSLOT = PAIR ? 5 : 8;
   static constexpr int SLOT = 16384;
-  static constexpr int KSUB = DH * BN * 2 / SLOT;   // K sub-tiles per key tile
-  static constexpr int KBOX = SLOT / (BN * 128);    // 64-column boxes per K sub-tile
-  static constexpr int VSUB = BN / 32;              // V sub-tiles (32 keys x 256 cols)
+  // K per CTA and tile: DUO holds 64 of the 128 keys, the others all BN keys.
+  static constexpr int KROWS = DUO ? 64 : BN;      // rows of a K box
+  static constexpr int KSUB = DH * KROWS * 2 / SLOT;  // K slots per tile
+  static constexpr int KBOX = SLOT / (KROWS * 128);   // 64-column K boxes per slot
+  // V per CTA and tile: DUO holds 128 of the 256 head-dim columns for all keys,
+  // in slots of 64 keys x 128 columns; the others hold slots of 32 keys x 256.
+  static constexpr int VROWS = DUO ? 64 : 32;      // keys per V slot (= rows of a V box)
+  static constexpr int VBOX = DUO ? 2 : 4;         // 64-column V boxes per slot
+  static constexpr int VSUB = BN / VROWS;          // V slots per tile
+  static constexpr int V_LBO = VROWS * 128;        // bytes between 64-column V boxes
   static constexpr int Q_OFF = 0;
   static constexpr int RING_OFF = 65536;
   static constexpr int P_OFF = RING_OFF + NSLOT * SLOT;
   static constexpr int P_BYTES = BM * BN * 2;
-  static constexpr int X_OFF = P_OFF + P_BYTES;
+  static constexpr int X_OFF = P_OFF + P_BYTES;      // peer's partial scores (received)
   static constexpr int X_BYTES = PAIR ? BM * BN * 4 : 0;
-  static constexpr int BAR_OFF = X_OFF + X_BYTES;
+  static constexpr int XS_OFF = X_OFF + X_BYTES;     // own partial scores (staged to send)
+  static constexpr int BAR_OFF = XS_OFF + X_BYTES;
   static constexpr int RED_OFF = BAR_OFF + 256;      // [2 parity][2 half][128 rows] floats
   static constexpr int SMEM_BYTES = RED_OFF + 2048;
   static constexpr int S_COL = 256;  // TMEM: O in columns [0,256), S buffers after it
   static constexpr int NTHREADS = 320;  // warps 0-7 softmax, 8 producer, 9 MMA
   static constexpr int kProducerWarp = 8;
   static constexpr int kMmaWarp = 9;
-  static constexpr uint32_t IDESC_QK = ptx::idesc_f16(128, BN, BF16, false, false);
-  static constexpr uint32_t IDESC_PV = ptx::idesc_f16(128, DH, BF16, false, true);
+  static constexpr int MMA_M = DUO ? 256 : 128;
+  static constexpr uint32_t IDESC_QK = ptx::idesc_f16(MMA_M, BN, BF16, false, false);
+  static constexpr uint32_t IDESC_PV = ptx::idesc_f16(MMA_M, DUO ? 2 * 128 : DH, BF16, false, true);
+  static constexpr int kSoftmaxArrivals = DUO ? 16 : 8;  // per-warp arrivals on S-empty / P-full
   static_assert(S_COL + 2 * BN <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(KSUB * KBOX * 64 == DH && VSUB * VROWS == BN, "tile decomposition");
 };
 
 // Barrier slots inside the barrier area.
@@ -123,8 +145,7 @@ enum {
   kBarXFull = 23,
   kBarXFree = 24,
   kBarDrain = 25,
-  kBarPair = 26,     // + lane quarter: row-max / row-sum exchange between the two halves
-  kNumBars = 30,
+  kNumBars = 26,
 };
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
@@ -135,11 +156,11 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          int* status, int code) {
-  if (kCluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity))
+  if (kCluster ? ptx::mbar_test_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity))
     return true;
   const uint64_t t0 = ptx::globaltimer();
-  for (uint32_t n = 1; n < (1u << 26); ++n) {
-    if (kCluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity))
+  for (uint32_t n = 1; n < (1u << 30); ++n) {
+    if (kCluster ? ptx::mbar_test_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity))
       return true;
     if ((n & 63) == 0) {
       if (*abort_flag) return false;
@@ -159,8 +180,12 @@ struct Work {
   int t_begin, t_step, t_count;
 };
 
-template <int BN>
-__device__ __forceinline__ Work make_work(const AttnParams& p, int item) {
+// Work of one CTA.  Prefill items walk (query head within its group, split, kv
+// head, batch, query tile) with the longest causal query tiles first; a query
+// tile has QROWS rows (256 for a 2-SM pair, of which CTA `rank` owns 128).
+// Decode items walk (head block, split, kv head, batch).
+template <int BN, int QROWS>
+__device__ __forceinline__ Work make_work(const AttnParams& p, int item, int rank) {
   Work w;
   int lo, hi;
   if (!p.decode) {
@@ -174,10 +199,11 @@ __device__ __forceinline__ Work make_work(const AttnParams& p, int item) {
     item /= p.B;
     const int qt = p.n_qtiles - 1 - item;  // longest causal tiles first
     w.h0 = w.hkv * p.G + hl;
-    w.m0 = qt * 128;
-    const int mlast = min(w.m0 + 128, p.Lq) - 1;
-    w.pmin = p.Lk - p.Lq + w.m0;
-    w.pmax = p.Lk - p.Lq + mlast;
+    const int q0 = qt * QROWS;
+    w.m0 = q0 + (QROWS == 256 ? rank * 128 : 0);
+    const int qlast = min(q0 + QROWS, p.Lq) - 1;
+    w.pmin = p.Lk - p.Lq + q0;
+    w.pmax = p.Lk - p.Lq + qlast;
     lo = (p.causal && p.window) ? max(0, w.pmin - p.window + 1) : 0;
     hi = p.causal ? min(p.Lk, w.pmax + 1) : p.Lk;
     const int tlo = lo / BN, thi = (hi + BN - 1) / BN;
@@ -218,9 +244,12 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
   }
 }
 
-template <bool BF16, bool PAIR>
+template <bool BF16, int MODE>
 __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
-  using C = Cfg<BF16, PAIR>;
+  using C = Cfg<BF16, MODE>;
+  constexpr bool PAIR = C::PAIR;
+  constexpr bool DUO = C::DUO;
+  constexpr bool CLUSTER = PAIR || DUO;
   constexpr int BN = C::BN;
   constexpr int HB = C::HB;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -244,10 +273,15 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
-  const int item = PAIR ? static_cast<int>(blockIdx.x / 2) : static_cast<int>(blockIdx.x);
-  const Work w = make_work<BN>(p, item);
-  const int d0 = static_cast<int>(rank) * C::DH;  // head-dim offset of this CTA
+  const uint32_t rank = CLUSTER ? ptx::cluster_ctarank() : 0u;
+  const uint32_t peer = rank ^ 1u;
+  const int item = CLUSTER ? static_cast<int>(blockIdx.x / 2) : static_cast<int>(blockIdx.x);
+  const Work w = make_work<BN, DUO ? 256 : 128>(p, item, static_cast<int>(rank));
+  const int d0 = PAIR ? static_cast<int>(rank) * C::DH : 0;  // head-dim offset of this CTA
+  // DUO: the pair's even CTA issues the MMAs and owns the barriers they wait on.
+  auto leader_bar = [&](int i) -> uint32_t {
+    return (DUO && rank != 0) ? ptx::mapa(bar(i), 0) : bar(i);
+  };
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(kBarQ), 1);
@@ -257,14 +291,13 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(bar(kBarSFull + b), 1);
-      ptx::mbar_init(bar(kBarSEmpty + b), 256);
+      ptx::mbar_init(bar(kBarSEmpty + b), C::kSoftmaxArrivals);
     }
-    ptx::mbar_init(bar(kBarPFull), 256);
+    ptx::mbar_init(bar(kBarPFull), C::kSoftmaxArrivals);
     ptx::mbar_init(bar(kBarPvDone), 1);
-    ptx::mbar_init(bar(kBarXFull), 256);
-    ptx::mbar_init(bar(kBarXFree), 256);
+    ptx::mbar_init(bar(kBarXFull), 1);  // local expect_tx arrive + the peer's bulk-copy bytes
+    ptx::mbar_init(bar(kBarXFree), 8);  // one arrive per softmax warp of the peer
     ptx::mbar_init(bar(kBarDrain), 1);
-    for (int q = 0; q < 4; ++q) ptx::mbar_init(bar(kBarPair + q), 64);
     *abort_flag = 0;
     ptx::fence_mbarrier_init();
   }
@@ -274,15 +307,21 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
     ptx::prefetch_tmap(&p.tm_v);
   }
   if (warp == C::kMmaWarp) {
-    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
-    ptx::tmem_relinquish();
+    if constexpr (DUO) {
+      ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), 512);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 512);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if (PAIR) ptx::cluster_sync();  // peer barriers initialised before any remote arrive
+  if (CLUSTER) ptx::cluster_sync();  // peer barriers initialised before any remote use
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int count = w.t_count;
+  const bool mma_cta = !DUO || rank == 0;  // this CTA issues MMAs
 
   // Producer / MMA bookkeeping kept for the drain after an abort.
   int issued_q = 0;
@@ -294,43 +333,61 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
     if (lane == 0 && count > 0) {
       const int bh_q = w.b * p.Hq + w.h0;
       const int bh_kv = w.b * p.Hkv + w.hkv;
+      auto load = [&](uint32_t dst, const CUtensorMap* m, uint32_t fullbar, int c0, int c1,
+                      int c2) {
+        if constexpr (DUO)
+          ptx::tma_load_3d_pair(dst, m, fullbar, c0, c1, c2);
+        else
+          ptx::tma_load_3d(dst, m, fullbar, c0, c1, c2);
+      };
       if (!p.decode) {
-        ptx::mbar_arrive_expect_tx(bar(kBarQ), 65536);
-        for (int c = 0; c < 4; ++c)
-          ptx::tma_load_3d(sQ + c * 16384, &p.tm_q, bar(kBarQ), d0 + c * 64, w.m0, bh_q);
+        const uint32_t qbar = leader_bar(kBarQ);
+        if (mma_cta) ptx::mbar_arrive_expect_tx(bar(kBarQ), DUO ? 2 * 65536 : 65536);
+        for (int c = 0; c < 4; ++c) load(sQ + c * 16384, &p.tm_q, qbar, d0 + c * 64, w.m0, bh_q);
         issued_q = 1;
       }
       uint32_t n = 0;  // ring sequence number
       bool ok = true;
+      auto next_slot = [&](int& slot, uint32_t& fullbar) -> bool {
+        slot = n % C::NSLOT;
+        if (!wait_bar(bar(kBarKvEmpty + slot), ((n / C::NSLOT) & 1) ^ 1, abort_flag, p.status,
+                      kDevTimeoutKvEmpty))
+          return false;
+        fullbar = leader_bar(kBarKvFull + slot);
+        // The MMA CTA posts the bytes of both halves (DUO) on its own barrier.
+        if (mma_cta) ptx::mbar_arrive_expect_tx(bar(kBarKvFull + slot), DUO ? 2 * C::SLOT : C::SLOT);
+        return true;
+      };
       auto load_k = [&](int j) {
-        const int key0 = (w.t_begin + j * w.t_step) * BN;
+        // DUO: CTA `rank` loads keys [64 rank, 64 rank + 64) of the 128-key tile.
+        const int key0 = (w.t_begin + j * w.t_step) * BN + (DUO ? static_cast<int>(rank) * 64 : 0);
         for (int ks = 0; ks < C::KSUB && ok; ++ks, ++n) {
-          const int slot = n % C::NSLOT;
-          if (!wait_bar(bar(kBarKvEmpty + slot), ((n / C::NSLOT) & 1) ^ 1, abort_flag, p.status,
-                        kDevTimeoutKvEmpty)) {
+          int slot;
+          uint32_t fb;
+          if (!next_slot(slot, fb)) {
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(bar(kBarKvFull + slot), C::SLOT);
           for (int e = 0; e < C::KBOX; ++e)
-            ptx::tma_load_3d(sRing + slot * C::SLOT + e * (BN * 128), &p.tm_k,
-                             bar(kBarKvFull + slot), d0 + (ks * C::KBOX + e) * 64, key0, bh_kv);
+            load(sRing + slot * C::SLOT + e * (C::KROWS * 128), &p.tm_k, fb,
+                 d0 + (ks * C::KBOX + e) * 64, key0, bh_kv);
           ring_issued = n + 1;
         }
       };
       auto load_v = [&](int j) {
+        // DUO: CTA `rank` loads head-dim columns [128 rank, 128 rank + 128) of V.
         const int key0 = (w.t_begin + j * w.t_step) * BN;
+        const int dv0 = DUO ? static_cast<int>(rank) * 128 : d0;
         for (int vs = 0; vs < C::VSUB && ok; ++vs, ++n) {
-          const int slot = n % C::NSLOT;
-          if (!wait_bar(bar(kBarKvEmpty + slot), ((n / C::NSLOT) & 1) ^ 1, abort_flag, p.status,
-                        kDevTimeoutKvEmpty)) {
+          int slot;
+          uint32_t fb;
+          if (!next_slot(slot, fb)) {
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(bar(kBarKvFull + slot), C::SLOT);
-          for (int c = 0; c < 4; ++c)
-            ptx::tma_load_3d(sRing + slot * C::SLOT + c * 4096, &p.tm_v, bar(kBarKvFull + slot),
-                             d0 + c * 64, key0 + vs * 32, bh_kv);
+          for (int c = 0; c < C::VBOX; ++c)
+            load(sRing + slot * C::SLOT + c * C::V_LBO, &p.tm_v, fb, dv0 + c * 64,
+                 key0 + vs * C::VROWS, bh_kv);
           ring_issued = n + 1;
         }
       };
@@ -343,10 +400,22 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
     }
   } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && count > 0) {
+    if (lane == 0 && count > 0 && mma_cta) {
       bool ok = wait_bar(bar(kBarQ), 0, abort_flag, p.status, kDevTimeoutQ);
       ptx::tc_fence_after();
       uint32_t n = 0;
+      auto mma = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+        if constexpr (DUO)
+          ptx::mma_f16_ss_pair(d, a, b, idesc, acc);
+        else
+          ptx::mma_f16_ss(d, a, b, idesc, acc);
+      };
+      auto commit = [&](int barid) {  // to this barrier in every CTA that waits on it
+        if constexpr (DUO)
+          ptx::mma_commit_pair_mc(bar(barid), 3);
+        else
+          ptx::mma_commit(bar(barid));
+      };
       auto consume = [&](uint32_t& slot_addr) -> bool {
         const int slot = n % C::NSLOT;
         if (!wait_bar(bar(kBarKvFull + slot), (n / C::NSLOT) & 1, abort_flag, p.status,
@@ -357,13 +426,13 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
         return true;
       };
       auto release = [&]() {
-        ptx::mma_commit(bar(kBarKvEmpty + (n % C::NSLOT)));
+        commit(kBarKvEmpty + static_cast<int>(n % C::NSLOT));
         ++n;
       };
       auto do_s = [&](int j) {
         const int buf = j & 1;
-        if (!wait_bar(bar(kBarSEmpty + buf), ((j >> 1) & 1) ^ 1, abort_flag, p.status,
-                      kDevTimeoutSEmpty)) {
+        if (!wait_bar<DUO>(bar(kBarSEmpty + buf), ((j >> 1) & 1) ^ 1, abort_flag, p.status,
+                           kDevTimeoutSEmpty)) {
           ok = false;
           return;
         }
@@ -381,17 +450,18 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t a = ptx::sdesc_sw128(sQ + dc * 16384 + kk * 32, 16, 1024);
-              const uint64_t b = ptx::sdesc_sw128(sk + e * (BN * 128) + kk * 32, 16, 1024);
-              ptx::mma_f16_ss(d_tmem, a, b, C::IDESC_QK, (dc | kk) != 0);
+              const uint64_t b =
+                  ptx::sdesc_sw128(sk + e * (C::KROWS * 128) + kk * 32, 16, 1024);
+              mma(d_tmem, a, b, C::IDESC_QK, (dc | kk) != 0);
             }
           }
           release();
           ++mma_issued;
         }
-        ptx::mma_commit(bar(kBarSFull + buf));
+        commit(kBarSFull + buf);
       };
       auto do_pv = [&](int j) {
-        if (!wait_bar(bar(kBarPFull), j & 1, abort_flag, p.status, kDevTimeoutPFull)) {
+        if (!wait_bar<DUO>(bar(kBarPFull), j & 1, abort_flag, p.status, kDevTimeoutPFull)) {
           ok = false;
           return;
         }
@@ -403,17 +473,17 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
             return;
           }
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            const int key = vs * 32 + kk * 16;
+          for (int kk = 0; kk < C::VROWS / 16; ++kk) {
+            const int key = vs * C::VROWS + kk * 16;
             const uint64_t a =
                 ptx::sdesc_sw128(sP + (key / 64) * 16384 + (key % 64) * 2, 16, 1024);
-            const uint64_t b = ptx::sdesc_sw128(sv + kk * 2048, 4096, 1024);
-            ptx::mma_f16_ss(tmem, a, b, C::IDESC_PV, (j | vs | kk) != 0);
+            const uint64_t b = ptx::sdesc_sw128(sv + kk * 2048, C::V_LBO, 1024);
+            mma(tmem, a, b, C::IDESC_PV, (j | vs | kk) != 0);
           }
           release();
           ++mma_issued;
         }
-        ptx::mma_commit(bar(kBarPvDone));
+        commit(kBarPvDone);
       };
       if (ok) do_s(0);
       for (int j = 1; j < count && ok; ++j) {
@@ -430,7 +500,6 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
     const int half = warp >> 2;
     const int t = q4 * 32 + lane;  // row of the tile == TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
-    const uint32_t pair_bar = bar(kBarPair + q4);
     int row_p;            // bottom-right position of this row
     bool row_valid;
     long long row_id;     // flat (b, h, i) row index, -1 if none
@@ -466,36 +535,50 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
         if (threadIdx.x == 0) ptx::mbar_arrive(bar(kBarQ));
       }
     }
+    // Per-warp arrival on a barrier the MMA issuer waits on (the pair's even
+    // CTA holds it in DUO mode).
+    auto warp_arrive = [&](int barid) {
+      __syncwarp();
+      if (lane == 0) {
+        if (DUO && rank != 0)
+          ptx::mbar_arrive_remote(ptx::mapa(bar(barid), 0));
+        else
+          ptx::mbar_arrive(bar(barid));
+      }
+    };
 
     const float c = p.c;
     float m_run = -INFINITY;  // running max of c * s (lazy: the true max may exceed it by < 8)
     float l = 0.f;            // this half's share of the row sum
-    bool ok = true;
-    const uint32_t peer = rank ^ 1u;
+    bool ok = true;      // false once the two halves of this row pair agree to stop
+    bool alive = true;   // false once a wait of this warp gave up
     int use = 0;  // pair-barrier uses so far
+    const uint32_t pair_id = 2 + q4;  // named barrier of warps q4 and q4 + 4
 
-    // Swap one float per row with the other half of the row (bounded wait).
+    // Swap one float per row with the other half of the row.  The named barrier
+    // also ANDs `alive` across the 64 threads, so both warps of a pair always
+    // take the same decision to stop and neither is left waiting at a barrier.
     auto swap_half = [&](float mine, float& other) -> bool {
       float* slot = red + (use & 1) * 256;
       slot[half * 128 + t] = mine;
-      ptx::mbar_arrive(pair_bar);
-      const bool got = __all_sync(0xffffffffu, wait_bar(pair_bar, use & 1, abort_flag, p.status,
-                                                         kDevTimeoutPair));
+      const bool both = ptx::bar_red_and(pair_id, 64, alive);
       other = slot[(half ^ 1) * 128 + t];
       ++use;
-      return got;
+      return both;
     };
 
-    for (int j = 0; j < count && ok; ++j) {
+    for (int j = 0; j < count; ++j) {
       const int tile = w.t_begin + j * w.t_step;
       const int kb = tile * BN + half * HB;  // first key of this thread's columns
       const int buf = j & 1;
-      ok = __all_sync(0xffffffffu, wait_bar(bar(kBarSFull + buf), (j >> 1) & 1, abort_flag,
-                                             p.status, kDevTimeoutSFull));
-      if (!ok) break;
-      ptx::tc_fence_after();
       float s[HB];
-      {
+#pragma unroll
+      for (int e = 0; e < HB; ++e) s[e] = -INFINITY;
+      if (alive)
+        alive = __all_sync(0xffffffffu, wait_bar(bar(kBarSFull + buf), (j >> 1) & 1, abort_flag,
+                                                 p.status, kDevTimeoutSFull));
+      if (alive) {
+        ptx::tc_fence_after();
         uint32_t r[HB / 32][32];
 #pragma unroll
         for (int cch = 0; cch < HB / 32; ++cch)
@@ -507,45 +590,59 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
 #pragma unroll
           for (int e = 0; e < 32; ++e) s[cch * 32 + e] = __uint_as_float(r[cch][e]);
         }
+        ptx::tc_fence_before();
+        warp_arrive(kBarSEmpty + buf);
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(kBarSEmpty + buf));
 
       if constexpr (PAIR) {
-        // Swap partial scores with the peer CTA (same columns) and add them.
-        ok = __all_sync(0xffffffffu, wait_bar<true>(bar(kBarXFree), (j & 1) ^ 1, abort_flag,
-                                                     p.status, kDevTimeoutXFree));
-        if (!ok) break;
-        const uint32_t rx = ptx::mapa(sX, peer) + t * (BN * 4);
+        // Swap partial scores with the peer CTA (same rows and columns) and add
+        // them.  Each warp stages its 32 rows x HB columns (4 KB) in XS and one
+        // lane bulk-copies the block into the peer's X, completing the bytes on
+        // the peer's XFull barrier; one local arrive per tile posts the expected
+        // byte count for the block the peer sends us.
+        const uint32_t wofs = static_cast<uint32_t>(warp) * (32 * HB * 4);
+        const uint32_t rofs = wofs + static_cast<uint32_t>(lane) * (HB * 4);
+        if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(bar(kBarXFull), C::X_BYTES);
+        if (alive)  // our previous block has been received and read by the peer
+          alive = __all_sync(0xffffffffu, wait_bar<true>(bar(kBarXFree), (j & 1) ^ 1,
+                                                         abort_flag, p.status, kDevTimeoutXFree));
+        if (alive) {
 #pragma unroll
-        for (int g = 0; g < HB / 4; ++g) {
-          const int gq = half * (HB / 4) + g;
-          const uint32_t off = ((gq ^ (t & 15)) << 4);
-          ptx::st_cluster_v4(rx + off, __float_as_uint(s[4 * g]), __float_as_uint(s[4 * g + 1]),
-                             __float_as_uint(s[4 * g + 2]), __float_as_uint(s[4 * g + 3]));
+          for (int g = 0; g < HB / 4; ++g) {
+            const uint32_t off = rofs + ((g ^ (lane & (HB / 4 - 1))) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + C::XS_OFF + off),
+                         "r"(__float_as_uint(s[4 * g])), "r"(__float_as_uint(s[4 * g + 1])),
+                         "r"(__float_as_uint(s[4 * g + 2])), "r"(__float_as_uint(s[4 * g + 3]))
+                         : "memory");
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0)
+            ptx::bulk_copy_to_peer(ptx::mapa(sX + wofs, peer), sbase + C::XS_OFF + wofs,
+                                   32 * HB * 4, ptx::mapa(bar(kBarXFull), peer));
+          alive = __all_sync(0xffffffffu, wait_bar<true>(bar(kBarXFull), j & 1, abort_flag,
+                                                         p.status, kDevTimeoutXFull));
         }
-        ptx::mbar_arrive_remote(ptx::mapa(bar(kBarXFull), peer));
-        ok = __all_sync(0xffffffffu, wait_bar<true>(bar(kBarXFull), j & 1, abort_flag, p.status,
-                                                     kDevTimeoutXFull));
-        if (!ok) break;
-        const uint32_t lx = sX + t * (BN * 4);
+        if (alive) {
 #pragma unroll
-        for (int g = 0; g < HB / 4; ++g) {
-          const int gq = half * (HB / 4) + g;
-          const uint32_t off = ((gq ^ (t & 15)) << 4);
-          float a0, a1, a2, a3;
-          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                       : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
-                       : "r"(lx + off)
-                       : "memory");
-          // rank 0 adds (own + peer), rank 1 adds (peer + own): the same two
-          // operands, so both CTAs hold bit-identical scores.
-          s[4 * g] += a0;
-          s[4 * g + 1] += a1;
-          s[4 * g + 2] += a2;
-          s[4 * g + 3] += a3;
+          for (int g = 0; g < HB / 4; ++g) {
+            const uint32_t off = rofs + ((g ^ (lane & (HB / 4 - 1))) << 4);
+            float a0, a1, a2, a3;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
+                         : "r"(sX + off)
+                         : "memory");
+            // rank 0 adds (own + peer), rank 1 adds (peer + own): the same two
+            // operands, so both CTAs hold bit-identical scores.
+            s[4 * g] += a0;
+            s[4 * g + 1] += a1;
+            s[4 * g + 2] += a2;
+            s[4 * g + 3] += a3;
+          }
+          // Our X block may be overwritten once this warp has read it.
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive_remote(ptx::mapa(bar(kBarXFree), peer));
         }
-        ptx::mbar_arrive_remote(ptx::mapa(bar(kBarXFree), peer));
       }
 
       // Mask (only on tiles that straddle the band edge or the end of the keys).
@@ -574,7 +671,7 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
       }
       float mo;
       ok = swap_half(mh, mo);
-      if (!ok) break;
+      if (!ok) break;  // both halves of the row stop together
       const float xm = fmaxf(mh, mo) * c;  // c > 0, so -inf stays -inf
       const bool grow = xm > m_run + 8.0f;
       const float m_old = m_run;
@@ -602,12 +699,13 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
       l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
 
       // The P buffer and O are free once the previous P.V product has completed.
-      if (j > 0) {
-        ok = __all_sync(0xffffffffu, wait_bar(bar(kBarPvDone), (j - 1) & 1, abort_flag,
-                                               p.status, kDevTimeoutPvDone));
-        if (!ok) break;
-        ptx::tc_fence_after();
-      }
+      if (j > 0 && alive)
+        alive = __all_sync(0xffffffffu, wait_bar(bar(kBarPvDone), (j - 1) & 1, abort_flag,
+                                                 p.status, kDevTimeoutPvDone));
+      // A warp whose wait gave up skips the rest of the tile; it stops together
+      // with its partner at the next swap.
+      if (!alive) continue;
+      ptx::tc_fence_after();
       if (__any_sync(0xffffffffu, rescale_o)) {
         const float a = rescale_o ? alpha : 1.f;
 #pragma unroll 1
@@ -635,22 +733,23 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
       }
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(kBarPFull));
+      warp_arrive(kBarPFull);
     }
 
     if (ok && count > 0) {
-      ok = __all_sync(0xffffffffu, wait_bar(bar(kBarPvDone), (count - 1) & 1, abort_flag,
-                                             p.status, kDevTimeoutPvDone));
+      if (alive)
+        alive = __all_sync(0xffffffffu, wait_bar(bar(kBarPvDone), (count - 1) & 1, abort_flag,
+                                                 p.status, kDevTimeoutPvDone));
       ptx::tc_fence_after();
       float lo = 0.f;
-      if (ok) ok = swap_half(l, lo);
+      ok = swap_half(l, lo);
       l = half == 0 ? l + lo : lo + l;  // both halves: l_0 + l_1
     }
     // ---------------------------------------------------------------- epilogue
     if (ok) {
       if (p.write_partial) {
         const long long R = static_cast<long long>(p.B) * p.Hq * p.Lq;
-        if (row_valid && half == 0 && rank == 0) {
+        if (row_valid && half == 0 && (!PAIR || rank == 0)) {
           const long long pr = static_cast<long long>(w.split) * R + row_id;
           p.part_ml[2 * pr] = m_run;
           p.part_ml[2 * pr + 1] = l;
@@ -705,9 +804,9 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
   if (*abort_flag) {
     // Let every copy and MMA this CTA started finish before its memory goes away.
     if (warp == C::kProducerWarp && lane == 0) {
-      if (issued_q) wait_bar(bar(kBarQ), 0, abort_flag, p.status, kDevTimeoutDrain);
+      if (issued_q && mma_cta) wait_bar(bar(kBarQ), 0, abort_flag, p.status, kDevTimeoutDrain);
       for (int s = 0; s < C::NSLOT; ++s)
-        if (static_cast<uint32_t>(s) < ring_issued) {
+        if (static_cast<uint32_t>(s) < ring_issued && mma_cta) {
           // the most recent load into slot s had sequence number `last`
           const uint32_t last = s + ((ring_issued - 1 - s) / C::NSLOT) * C::NSLOT;
           const uint32_t ph = (last / C::NSLOT) & 1;
@@ -718,68 +817,106 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
         }
     }
     if (warp == C::kMmaWarp && lane == 0 && mma_issued) {
-      ptx::mma_commit(bar(kBarDrain));
+      if constexpr (DUO)
+        ptx::mma_commit_pair_mc(bar(kBarDrain), 1);
+      else
+        ptx::mma_commit(bar(kBarDrain));
       const uint64_t t0 = ptx::globaltimer();
       while (!ptx::mbar_try_wait(bar(kBarDrain), 0) && ptx::globaltimer() - t0 < kTimeoutNs) {
       }
     }
     __syncthreads();
   }
-  if (PAIR) ptx::cluster_sync();  // peer may still write into our X buffer until here
+  // The peer may still write into our shared memory (PAIR) or read our tiles and
+  // tensor memory through 2-SM MMAs (DUO) until both CTAs get here.
+  if (CLUSTER) ptx::cluster_sync();
   if (warp == C::kMmaWarp) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, 512);
+    if constexpr (DUO)
+      ptx::tmem_dealloc_pair(tmem, 512);
+    else
+      ptx::tmem_dealloc(tmem, 512);
   }
 }
 
 // Merge split partials: for each row, M = max_s m_s, l = sum_s 2^(m_s - M) l_s,
-// out = sum_s 2^(m_s - M) O_s / l, splits taken in increasing order, splits
-// that saw no visible key (l_s == 0) skipped.  One CTA per row; the maximum is
-// a warp-shuffle reduction, the weighted sums run in a fixed order, so a row's
-// result depends only on that row's partials.
+// out = sum_s 2^(m_s - M) O_s / l, splits that saw no visible key (l_s == 0)
+// skipped.  Grid (rows, D / 128); 256 threads: warp w accumulates splits
+// w, w+8, w+16, ... for 128 columns (4 per lane), then the eight warp sums are
+// added in warp order.  The maximum is a warp-shuffle reduction; every sum runs
+// in a fixed order, so a row's result depends only on that row's partials.
+constexpr int kCombineThreads = 256;
+
 template <bool BF16>
-__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ part_o,
-                                                      const float* __restrict__ part_ml,
-                                                      uint16_t* __restrict__ out, long long R,
-                                                      int D, int n_splits) {
-  extern __shared__ float wts[];  // n_splits weights, then the total l
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(
+    const float* __restrict__ part_o, const float* __restrict__ part_ml,
+    uint16_t* __restrict__ out, long long R, int D, int n_splits) {
+  extern __shared__ float sm[];
+  float* wts = sm;                          // [n_splits] weights, then the total l
+  float4* acc_w = reinterpret_cast<float4*>(sm + ((n_splits + 4) & ~3));  // [8][32]
   const long long row = blockIdx.x;
-  const int t = threadIdx.x;
-  if (t < 32) {
+  const int c0 = blockIdx.y * 128;
+  const int t = threadIdx.x, warp = t / 32, lane = t % 32;
+  if (warp == 0) {
     float mx = -INFINITY;
-    for (int s = t; s < n_splits; s += 32) {
-      const float ls = part_ml[2 * (s * R + row) + 1];
-      if (ls > 0.f) mx = fmaxf(mx, part_ml[2 * (s * R + row)]);
+    for (int s = lane; s < n_splits; s += 32) {
+      const float2 ml = *reinterpret_cast<const float2*>(part_ml + 2 * (s * R + row));
+      if (ml.y > 0.f) mx = fmaxf(mx, ml.x);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    for (int s = t; s < n_splits; s += 32) {
-      const float ms = part_ml[2 * (s * R + row)];
-      const float ls = part_ml[2 * (s * R + row) + 1];
-      wts[s] = ls > 0.f ? ptx::ex2(ms - mx) : 0.f;
+    for (int s = lane; s < n_splits; s += 32) {
+      const float2 ml = *reinterpret_cast<const float2*>(part_ml + 2 * (s * R + row));
+      wts[s] = ml.y > 0.f ? ptx::ex2(ml.x - mx) : 0.f;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      float lt = 0.f;
+      for (int s = 0; s < n_splits; ++s)
+        if (wts[s] != 0.f) lt += wts[s] * part_ml[2 * (s * R + row) + 1];
+      wts[n_splits] = lt;
     }
   }
   __syncthreads();
-  if (t == 0) {
-    float lt = 0.f;
-    for (int s = 0; s < n_splits; ++s)
-      if (wts[s] != 0.f) lt += wts[s] * part_ml[2 * (s * R + row) + 1];
-    wts[n_splits] = lt;
-  }
-  __syncthreads();
-  const float lt = wts[n_splits];
-  const float inv = lt > 0.f ? 1.f / lt : 0.f;
-  for (int d = 2 * t; d < D; d += 256) {
-    float a0 = 0.f, a1 = 0.f;
-    for (int s = 0; s < n_splits; ++s) {
-      const float ws = wts[s];
-      if (ws != 0.f) {
-        const float2 v = *reinterpret_cast<const float2*>(part_o + (s * R + row) * D + d);
-        a0 = fmaf(ws, v.x, a0);
-        a1 = fmaf(ws, v.y, a1);
-      }
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float* base = part_o + row * D + c0 + 4 * lane;
+  const long long split_stride = R * D;
+  for (int s0 = warp; s0 < n_splits; s0 += 8 * 4) {
+    float4 v[4];
+    float wv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int s = s0 + 8 * u;
+      wv[u] = s < n_splits ? wts[s] : 0.f;
+      v[u] = wv[u] != 0.f ? *reinterpret_cast<const float4*>(base + s * split_stride)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    *reinterpret_cast<uint32_t*>(out + row * D + d) = pack2(a0 * inv, a1 * inv, BF16);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      a.x = fmaf(wv[u], v[u].x, a.x);
+      a.y = fmaf(wv[u], v[u].y, a.y);
+      a.z = fmaf(wv[u], v[u].z, a.z);
+      a.w = fmaf(wv[u], v[u].w, a.w);
+    }
+  }
+  acc_w[warp * 32 + lane] = a;
+  __syncthreads();
+  if (warp == 0) {
+    float4 sum = acc_w[lane];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) {
+      const float4 b = acc_w[w * 32 + lane];
+      sum.x += b.x;
+      sum.y += b.y;
+      sum.z += b.z;
+      sum.w += b.w;
+    }
+    const float lt = wts[n_splits];
+    const float inv = lt > 0.f ? 1.f / lt : 0.f;
+    uint2 o;
+    o.x = pack2(sum.x * inv, sum.y * inv, BF16);
+    o.y = pack2(sum.z * inv, sum.w * inv, BF16);
+    *reinterpret_cast<uint2*>(out + row * D + c0 + 4 * lane) = o;
   }
 }
 
