@@ -158,11 +158,14 @@ size_t partial_bytes(long long R, int D, int n_splits) {
 }
 
 // Kernel variant for a call: head_dim 512 splits the head dimension over a CTA
-// pair; head_dim 256 prefill uses 2-SM MMAs over 256-row query tiles; decode
+// pair; head_dim 256 prefill uses 2-SM MMAs over 256-row query tiles, except
+// with a sliding window shorter than 4096 keys, where a 256-row tile would add
+// too many masked keys and 128-row tiles on one CTA each do less work; decode
 // uses one CTA per 16 query heads x 8 position slots.
-int choose_mode(bool decode, int D) {
+int choose_mode(bool decode, int D, int window) {
   if (D == 512) return gbsdpa::kPair;
-  return decode ? gbsdpa::kSingle : gbsdpa::kDuo;
+  if (decode) return gbsdpa::kSingle;
+  return (window > 0 && window < 4096) ? gbsdpa::kSingle : gbsdpa::kDuo;
 }
 
 int qtile_rows(int mode) { return mode == gbsdpa::kDuo ? 256 : 128; }
@@ -182,7 +185,7 @@ long long max_tiles_per_qtile(int Lq, int Lk, int causal, int window, int bn, in
 // simple wave model: time ~ ceil(ctas / sms) * ceil(tiles / s), plus the cost
 // of writing and re-reading the fp32 partials.
 int plan_prefill_splits(int sms, int B, int Hq, int Lq, int Lk, int D, int causal, int window) {
-  const int mode = choose_mode(false, D);
+  const int mode = choose_mode(false, D, causal ? window : 0);
   const int bn = key_tile(mode), rows = qtile_rows(mode);
   const long long items = static_cast<long long>(B) * Hq * ((Lq + rows - 1) / rows);
   const long long per_cta = mode == gbsdpa::kSingle ? 1 : 2;
@@ -222,7 +225,7 @@ int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, i
         bool write_partial, void* workspace, cudaStream_t stream, DeviceState* st) {
   AttnParams p;
   std::memset(&p, 0, sizeof(p));
-  const int mode = choose_mode(decode, D);
+  const int mode = choose_mode(decode, D, window);
   // K boxes: all keys of a tile (one CTA), or the CTA's 64 keys (pair kernels);
   // V boxes: 32 keys (one CTA, head-dim split) or 64 keys (2-SM MMA).
   const int k_rows = mode == gbsdpa::kSingle ? 128 : 64;

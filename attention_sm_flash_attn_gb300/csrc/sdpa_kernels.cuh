@@ -127,7 +127,9 @@ struct Cfg {
   static constexpr int MMA_M = DUO ? 256 : 128;
   static constexpr uint32_t IDESC_QK = ptx::idesc_f16(MMA_M, BN, BF16, false, false);
   static constexpr uint32_t IDESC_PV = ptx::idesc_f16(MMA_M, DUO ? 2 * 128 : DH, BF16, false, true);
-  static constexpr int kSoftmaxArrivals = DUO ? 16 : 8;  // per-warp arrivals on S-empty / P-full
+  // Arrivals completing P-full on the MMA CTA: one per softmax warp, plus (DUO)
+  // one forwarded from the other CTA of the pair.
+  static constexpr int kPFullArrivals = DUO ? 9 : 8;
   static_assert(S_COL + 2 * BN <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(KSUB * KBOX * 64 == DH && VSUB * VROWS == BN, "tile decomposition");
@@ -139,7 +141,7 @@ enum {
   kBarKvFull = 1,    // + slot (8 slots max)
   kBarKvEmpty = 9,   // + slot
   kBarSFull = 17,    // + buf
-  kBarSEmpty = 19,   // + buf
+  kBarPFullPeer = 19,  // DUO, odd CTA: its own softmax warps' P-ready arrivals
   kBarPFull = 21,
   kBarPvDone = 22,
   kBarXFull = 23,
@@ -289,11 +291,9 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
       ptx::mbar_init(bar(kBarKvFull + s), 1);
       ptx::mbar_init(bar(kBarKvEmpty + s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(bar(kBarSFull + b), 1);
-      ptx::mbar_init(bar(kBarSEmpty + b), C::kSoftmaxArrivals);
-    }
-    ptx::mbar_init(bar(kBarPFull), C::kSoftmaxArrivals);
+    for (int b = 0; b < 2; ++b) ptx::mbar_init(bar(kBarSFull + b), 1);
+    ptx::mbar_init(bar(kBarPFull), C::kPFullArrivals);
+    ptx::mbar_init(bar(kBarPFullPeer), 8);
     ptx::mbar_init(bar(kBarPvDone), 1);
     ptx::mbar_init(bar(kBarXFull), 1);  // local expect_tx arrive + the peer's bulk-copy bytes
     ptx::mbar_init(bar(kBarXFree), 8);  // one arrive per softmax warp of the peer
@@ -400,6 +400,14 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
     }
   } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
+    if (DUO && lane == 0 && count > 0 && !mma_cta) {
+      // Odd CTA of a 2-SM pair: forward "P_j is in shared memory" to the even CTA.
+      const uint32_t remote = ptx::mapa(bar(kBarPFull), 0);
+      for (int j = 0; j < count; ++j) {
+        if (!wait_bar(bar(kBarPFullPeer), j & 1, abort_flag, p.status, kDevTimeoutPFull)) break;
+        ptx::mbar_arrive_remote(remote);
+      }
+    }
     if (lane == 0 && count > 0 && mma_cta) {
       bool ok = wait_bar(bar(kBarQ), 0, abort_flag, p.status, kDevTimeoutQ);
       ptx::tc_fence_after();
@@ -430,13 +438,9 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
         ++n;
       };
       auto do_s = [&](int j) {
+        // S buffer j % 2 last held S_{j-2}; the softmax read it before it
+        // produced P_{j-2}, and do_pv(j - 2) has already waited for P_{j-2}.
         const int buf = j & 1;
-        if (!wait_bar<DUO>(bar(kBarSEmpty + buf), ((j >> 1) & 1) ^ 1, abort_flag, p.status,
-                           kDevTimeoutSEmpty)) {
-          ok = false;
-          return;
-        }
-        ptx::tc_fence_after();
         const uint32_t d_tmem = tmem + C::S_COL + buf * BN;
         for (int ks = 0; ks < C::KSUB; ++ks) {
           uint32_t sk;
@@ -535,16 +539,13 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
         if (threadIdx.x == 0) ptx::mbar_arrive(bar(kBarQ));
       }
     }
-    // Per-warp arrival on a barrier the MMA issuer waits on (the pair's even
-    // CTA holds it in DUO mode).
-    auto warp_arrive = [&](int barid) {
+    // Per-warp arrival telling the MMA issuer that this warp's P rows are in
+    // shared memory.  In the odd CTA of a 2-SM pair the arrival stays local and
+    // that CTA's MMA warp forwards one cluster-scope arrival per tile to the even
+    // CTA, keeping the slow cluster-scope release off the softmax warps.
+    auto warp_arrive_p = [&]() {
       __syncwarp();
-      if (lane == 0) {
-        if (DUO && rank != 0)
-          ptx::mbar_arrive_remote(ptx::mapa(bar(barid), 0));
-        else
-          ptx::mbar_arrive(bar(barid));
-      }
+      if (lane == 0) ptx::mbar_arrive(bar((DUO && rank != 0) ? kBarPFullPeer : kBarPFull));
     };
 
     const float c = p.c;
@@ -590,8 +591,6 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
 #pragma unroll
           for (int e = 0; e < 32; ++e) s[cch * 32 + e] = __uint_as_float(r[cch][e]);
         }
-        ptx::tc_fence_before();
-        warp_arrive(kBarSEmpty + buf);
       }
 
       if constexpr (PAIR) {
@@ -733,7 +732,7 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
       }
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
-      warp_arrive(kBarPFull);
+      warp_arrive_p();
     }
 
     if (ok && count > 0) {
