@@ -50,6 +50,14 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
                : "memory");
 }
 
+// Arrive on an mbarrier of another CTA of the cluster with the default (CTA
+// scope) release.  For signals that only hand a buffer back to its writer
+// after this thread's reads of it (the reads complete before the arrive issues),
+// where no data written by this thread has to become visible to the other CTA.
+__device__ __forceinline__ void mbar_arrive_remote_free(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(

@@ -640,7 +640,7 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
           }
           // Our X block may be overwritten once this warp has read it.
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive_remote(ptx::mapa(bar(kBarXFree), peer));
+          if (lane == 0) ptx::mbar_arrive_remote_free(ptx::mapa(bar(kBarXFree), peer));
         }
       }
 
