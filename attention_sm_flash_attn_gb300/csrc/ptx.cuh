@@ -51,10 +51,12 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
 }
 
 // Arrive on an mbarrier of another CTA of the cluster with the default (CTA
-// scope) release.  For signals that only hand a buffer back to its writer
-// after this thread's reads of it (the reads complete before the arrive issues),
-// where no data written by this thread has to become visible to the other CTA.
-__device__ __forceinline__ void mbar_arrive_remote_free(uint32_t cluster_bar) {
+// scope) release.  Used where no data written by this thread has to become
+// visible to threads of the other CTA: handing a buffer back to its writer after
+// this thread's reads of it (reads complete before the arrive issues), or
+// announcing shared-memory operands that this CTA's own SM will read through
+// the async proxy (made visible to it by fence.proxy.async before the arrive).
+__device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 

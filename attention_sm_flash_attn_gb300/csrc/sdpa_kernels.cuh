@@ -127,9 +127,9 @@ struct Cfg {
   static constexpr int MMA_M = DUO ? 256 : 128;
   static constexpr uint32_t IDESC_QK = ptx::idesc_f16(MMA_M, BN, BF16, false, false);
   static constexpr uint32_t IDESC_PV = ptx::idesc_f16(MMA_M, DUO ? 2 * 128 : DH, BF16, false, true);
-  // Arrivals completing P-full on the MMA CTA: one per softmax warp, plus (DUO)
-  // one forwarded from the other CTA of the pair.
-  static constexpr int kPFullArrivals = DUO ? 9 : 8;
+  // Arrivals completing P-full on the MMA CTA: one per softmax warp of each CTA
+  // whose P rows the MMA reads.
+  static constexpr int kPFullArrivals = DUO ? 16 : 8;
   static_assert(S_COL + 2 * BN <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(KSUB * KBOX * 64 == DH && VSUB * VROWS == BN, "tile decomposition");
@@ -141,7 +141,6 @@ enum {
   kBarKvFull = 1,    // + slot (8 slots max)
   kBarKvEmpty = 9,   // + slot
   kBarSFull = 17,    // + buf
-  kBarPFullPeer = 19,  // DUO, odd CTA: its own softmax warps' P-ready arrivals
   kBarPFull = 21,
   kBarPvDone = 22,
   kBarXFull = 23,
@@ -293,7 +292,6 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
     }
     for (int b = 0; b < 2; ++b) ptx::mbar_init(bar(kBarSFull + b), 1);
     ptx::mbar_init(bar(kBarPFull), C::kPFullArrivals);
-    ptx::mbar_init(bar(kBarPFullPeer), 8);
     ptx::mbar_init(bar(kBarPvDone), 1);
     ptx::mbar_init(bar(kBarXFull), 1);  // local expect_tx arrive + the peer's bulk-copy bytes
     ptx::mbar_init(bar(kBarXFree), 8);  // one arrive per softmax warp of the peer
@@ -400,14 +398,6 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
     }
   } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (DUO && lane == 0 && count > 0 && !mma_cta) {
-      // Odd CTA of a 2-SM pair: forward "P_j is in shared memory" to the even CTA.
-      const uint32_t remote = ptx::mapa(bar(kBarPFull), 0);
-      for (int j = 0; j < count; ++j) {
-        if (!wait_bar(bar(kBarPFullPeer), j & 1, abort_flag, p.status, kDevTimeoutPFull)) break;
-        ptx::mbar_arrive_remote(remote);
-      }
-    }
     if (lane == 0 && count > 0 && mma_cta) {
       bool ok = wait_bar(bar(kBarQ), 0, abort_flag, p.status, kDevTimeoutQ);
       ptx::tc_fence_after();
@@ -540,12 +530,18 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
       }
     }
     // Per-warp arrival telling the MMA issuer that this warp's P rows are in
-    // shared memory.  In the odd CTA of a 2-SM pair the arrival stays local and
-    // that CTA's MMA warp forwards one cluster-scope arrival per tile to the even
-    // CTA, keeping the slow cluster-scope release off the softmax warps.
+    // shared memory.  In the odd CTA of a 2-SM pair the barrier is the even
+    // CTA's; the P rows stay in this CTA and are read by this SM's tensor core
+    // (the fence.proxy.async before the arrive makes them visible to it), so a
+    // CTA-scope release suffices and avoids the cost of a cluster-scope one.
     auto warp_arrive_p = [&]() {
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar((DUO && rank != 0) ? kBarPFullPeer : kBarPFull));
+      if (lane == 0) {
+        if (DUO && rank != 0)
+          ptx::mbar_arrive_remote_cta(ptx::mapa(bar(kBarPFull), 0));
+        else
+          ptx::mbar_arrive(bar(kBarPFull));
+      }
     };
 
     const float c = p.c;
@@ -640,7 +636,7 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
           }
           // Our X block may be overwritten once this warp has read it.
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive_remote_free(ptx::mapa(bar(kBarXFree), peer));
+          if (lane == 0) ptx::mbar_arrive_remote_cta(ptx::mapa(bar(kBarXFree), peer));
         }
       }
 
