@@ -25,7 +25,7 @@ __all__ = [
 SDPA_F16, SDPA_BF16 = 0, 1
 EXPORTED_SYMBOLS = ("sdpa_prefill", "sdpa_prefill_workspace_bytes", "sdpa_decode",
                     "sdpa_decode_workspace_bytes", "sdpa_device_status", "sdpa_status_string",
-                    "sdpa_version", "sdpa_decode_noalloc")
+                    "sdpa_version", "sdpa_decode_noalloc", "sdpa_selftest_timeout")
 # Size of the library-resident scratch used by sdpa_decode_noalloc (see the header).
 NOALLOC_SCRATCH_BYTES = 24 << 20
 
@@ -71,6 +71,9 @@ def load_library(path: str | None = None):
         lib.sdpa_version.restype = i
         lib.sdpa_decode_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, i, vp]
         lib.sdpa_decode_noalloc.restype = i
+        lib.sdpa_selftest_timeout.argtypes = [vp, vp, vp, vp, i, i, vp, sz, vp,
+                                              ctypes.POINTER(i)]
+        lib.sdpa_selftest_timeout.restype = i
         if path == _build.LIB_PATH:
             _lib = lib
         return lib

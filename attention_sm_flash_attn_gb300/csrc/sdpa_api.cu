@@ -222,7 +222,8 @@ int plan_decode_splits(int sms, int B, int Hq, int Hkv, int D) {
 template <bool BF16>
 int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv, int Lq,
         int Lk, int D, float scale, int causal, int window, bool decode, int n_splits,
-        bool write_partial, void* workspace, cudaStream_t stream, DeviceState* st) {
+        bool write_partial, void* workspace, cudaStream_t stream, DeviceState* st,
+        int withhold_q = 0) {
   AttnParams p;
   std::memset(&p, 0, sizeof(p));
   const int mode = choose_mode(decode, D, window);
@@ -264,6 +265,7 @@ int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, i
   p.n_splits = n_splits;
   p.n_hb = (p.G + 15) / 16;
   p.write_partial = write_partial ? 1 : 0;
+  p.withhold_q = withhold_q;
   long long items;
   if (decode)
     items = static_cast<long long>(B) * Hkv * n_splits * p.n_hb;
@@ -382,6 +384,30 @@ const char* sdpa_status_string(int status) {
 }
 
 int sdpa_version(void) { return 100; }
+
+int sdpa_selftest_timeout(const void* q, const void* k, const void* v, void* out, int D,
+                          int decode, void* workspace, size_t workspace_bytes,
+                          sdpa_stream_t stream, int* detail) {
+  if (detail) *detail = 0;
+  if (!q || !k || !v || !out || (D != 256 && D != 512)) return SDPA_ERR_INVALID_ARG;
+  const int B = 1, Hq = 2, Hkv = 1, Lq = decode ? 1 : 128, Lk = 128;
+  int rc = validate(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, 1.f / 16.f, 1, 0, SDPA_F16);
+  if (rc) return rc;
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc) return rc;
+  auto strm = reinterpret_cast<cudaStream_t>(stream);
+  int s = 1;
+  if (decode) {
+    s = plan_decode_splits(st->sms, B, Hq, Hkv, D);
+    if (!workspace || workspace_bytes < partial_bytes(static_cast<long long>(B) * Hq * Lq, D, s))
+      return SDPA_ERR_WORKSPACE;
+  }
+  rc = run<false>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, 1.f / 16.f, 1, 0, decode != 0, s,
+                  decode != 0, workspace, strm, st, /*withhold_q=*/1);
+  if (rc) return rc;
+  return sdpa_device_status(stream, detail);
+}
 
 }  // extern "C"
 

@@ -79,6 +79,10 @@ struct AttnParams {
   int n_splits;   // prefill: 1 => final output written directly; decode: fixed split count
   int n_hb;       // decode: query-head blocks of 16 per kv head
   int write_partial;
+  // Self-test only (always 0 on the normal entry points): 1 = withhold the
+  // "query tile ready" signal, so the MMA issuer's bounded wait runs out and the
+  // kernel reports a device timeout instead of computing.
+  int withhold_q;
 };
 
 // Kernel variants.
@@ -338,7 +342,7 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
         else
           ptx::tma_load_3d(dst, m, fullbar, c0, c1, c2);
       };
-      if (!p.decode) {
+      if (!p.decode && !p.withhold_q) {
         const uint32_t qbar = leader_bar(kBarQ);
         if (mma_cta) ptx::mbar_arrive_expect_tx(bar(kBarQ), DUO ? 2 * 65536 : 65536);
         for (int c = 0; c < 4; ++c) load(sQ + c * 16384, &p.tm_q, qbar, d0 + c * 64, w.m0, bh_q);
@@ -526,7 +530,7 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
         }
         ptx::fence_proxy_async_smem();
         asm volatile("bar.sync 1, 256;" ::: "memory");
-        if (threadIdx.x == 0) ptx::mbar_arrive(bar(kBarQ));
+        if (threadIdx.x == 0 && !p.withhold_q) ptx::mbar_arrive(bar(kBarQ));
       }
     }
     // Per-warp arrival telling the MMA issuer that this warp's P rows are in

@@ -292,6 +292,17 @@ def profile_run(args):
     return 0 if st[0] == 0 else 1
 
 
+# ---------------------------------------------------------------- ranks
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest `value` over all ranks (the job's time is its slowest rank's)."""
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ---------------------------------------------------------------- main
 
 def dist_setup(args):
@@ -314,7 +325,8 @@ def run_reference(args, world, rank):
     vals = []
     cb = None
     for step in range(args.warmup + args.steps):
-        cb = cpu_baseline(w, q, k, v, budget_s=6.0 if step >= args.warmup else 1.0)
+        cb = cpu_baseline(w, q, k, v,
+                          budget_s=args.cpu_budget if step >= args.warmup else args.cpu_budget / 6)
         if step >= args.warmup:
             vals.append(cb["value"])
     value = statistics.median(vals)
@@ -342,6 +354,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-suite", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=6.0,
+                    help="seconds of oracle work per timed step of the reference arm")
     ap.add_argument("--profile", default=None,
                     help="run one named workload --steps times (for ncu) and exit; decode "
                          "workloads take a _LqN suffix")
@@ -389,11 +403,7 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     clk = clocks.stop()
-    total_ms = sum(ts)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(ts), dist, device)
     status = gb.device_status()
     ms_per_step = total_ms / args.steps
     value = world * flops * args.steps / (total_ms * 1e9)  # TFLOP/s, all ranks

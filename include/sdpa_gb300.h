@@ -135,6 +135,23 @@ const char* sdpa_status_string(int status);
 int sdpa_version(void);
 
 /*
+ * Self-test of the device-side failure path: runs one small fp16 call
+ * (B = 1, Hq = 2, Hkv = 1, Lk = 128, head_dim D in {256, 512}; prefill with
+ * Lq = 128, or decode with Lq = 1 when `decode` is 1) in which the "query tile
+ * ready" signal is deliberately withheld.  The kernel's bounded wait for it
+ * gives up after about 2 s, every CTA drains its copies and MMAs and exits, and
+ * the call returns what sdpa_device_status() then reports:
+ * SDPA_ERR_DEVICE_TIMEOUT, with *detail the code (0x100..0x10a) of the first
+ * wait that gave up: the query-tile wait itself (0x100) or one that depends on
+ * it.  No fault, trap or hang is involved; the CUDA context stays usable.
+ * q, k, v, out: device buffers of the shapes above ([1,2,Lq,D], [1,1,128,D]);
+ * decode also needs a workspace of sdpa_decode_workspace_bytes(1, 2, 1, 1, D).
+ */
+int sdpa_selftest_timeout(const void* q, const void* k, const void* v, void* out, int D,
+                          int decode, void* workspace, size_t workspace_bytes,
+                          sdpa_stream_t stream, int* detail);
+
+/*
  * sdpa_decode_noalloc -- sdpa_decode for callers that cannot allocate device
  * memory.  (The paper, i.e. the web pages this library follows, has no
  * counterpart of this entry point; it is a convenience of this library.)
