@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <chrono>
 #include <cmath>
 #include <cstring>
 #include <cstdint>
@@ -28,6 +29,8 @@ struct DeviceState {
   int sms = 0;
   int* status = nullptr;  // device address of g_device_status
   bool attr_set[6] = {false, false, false, false, false, false};
+  int sk_units[6] = {0, 0, 0, 0, 0, 0};  // resident persistent units per variant
+  unsigned long long epoch = 0;          // last persistent-launch epoch handed out
 };
 
 std::mutex g_mu;
@@ -45,6 +48,11 @@ int device_state(DeviceState** out) {
     void* addr = nullptr;
     if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) return SDPA_ERR_CUDA;
     st.status = static_cast<int*>(addr);
+    // Suffix-piece flags hold the epoch of the launch that wrote them.  Start from a
+    // clock-derived value so that a workspace left over from another process
+    // can never hold the epoch of a launch of this one.
+    const auto now = std::chrono::steady_clock::now().time_since_epoch().count();
+    st.epoch = (static_cast<unsigned long long>(now) * 0x9E3779B97F4A7C15ull) >> 1;
     if (!g_encode) {
       cudaDriverEntryPointQueryResult q;
       void* fn = nullptr;
@@ -111,28 +119,81 @@ int ensure_attr(DeviceState* st) {
 }
 
 template <bool BF16, int MODE>
+void fill_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, long long ctas,
+                 cudaStream_t stream, bool cooperative) {
+  constexpr bool kCluster = MODE != gbsdpa::kSingle;
+  *cfg = {};
+  cfg->gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+  cfg->blockDim = dim3(Cfg<BF16, MODE>::NTHREADS, 1, 1);
+  cfg->dynamicSmemBytes = Cfg<BF16, MODE>::SMEM_BYTES;
+  cfg->stream = stream;
+  cfg->attrs = attr;
+  cfg->numAttrs = 0;
+  if (kCluster) {
+    attr[cfg->numAttrs].id = cudaLaunchAttributeClusterDimension;
+    attr[cfg->numAttrs].val.clusterDim.x = 2;
+    attr[cfg->numAttrs].val.clusterDim.y = 1;
+    attr[cfg->numAttrs].val.clusterDim.z = 1;
+    ++cfg->numAttrs;
+  }
+  if (cooperative) {
+    attr[cfg->numAttrs].id = cudaLaunchAttributeCooperative;
+    attr[cfg->numAttrs].val.cooperative = 1;
+    ++cfg->numAttrs;
+  }
+}
+
+template <bool BF16, int MODE>
 int launch_attn(const AttnParams& p, long long items, cudaStream_t stream, DeviceState* st) {
   int rc = ensure_attr<BF16, MODE>(st);
   if (rc) return rc;
   constexpr bool kCluster = MODE != gbsdpa::kSingle;
   const long long ctas = items * (kCluster ? 2 : 1);
   if (ctas <= 0 || ctas > 0x7fffffffll) return SDPA_ERR_INVALID_ARG;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
-  cfg.blockDim = dim3(Cfg<BF16, MODE>::NTHREADS, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<BF16, MODE>::SMEM_BYTES;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  if (kCluster) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-  }
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[2];
+  // A persistent grid waits on itself, so all of its CTAs must be resident at
+  // once: ask for a cooperative launch, which refuses a grid that cannot be.
+  fill_launch<BF16, MODE>(&cfg, attr, ctas, stream, p.persistent != 0);
   cudaError_t e = cudaLaunchKernelEx(&cfg, gbsdpa::attn_fwd_kernel<BF16, MODE>, p);
+  if (e != cudaSuccess && p.persistent) {
+    // Cooperative launches of clusters may be refused.  The grid is already
+    // sized to the occupancy limit, and a unit that never became resident would
+    // only make its owner's bounded wait report a timeout.
+    (void)cudaGetLastError();
+    fill_launch<BF16, MODE>(&cfg, attr, ctas, stream, false);
+    e = cudaLaunchKernelEx(&cfg, gbsdpa::attn_fwd_kernel<BF16, MODE>, p);
+  }
   return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+// How many persistent units (CTAs, or CTA pairs for the 2-SM variant) can be
+// resident at once on this device; 0 if the variant cannot run persistently.
+template <bool BF16, int MODE>
+int resident_units(DeviceState* st) {
+  const int idx = (BF16 ? 1 : 0) + 2 * MODE;
+  if (st->sk_units[idx]) return st->sk_units[idx];
+  if (ensure_attr<BF16, MODE>(st)) return 0;
+  int units = 0;
+  if (MODE == gbsdpa::kSingle) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gbsdpa::attn_fwd_kernel<BF16, MODE>,
+                                                      Cfg<BF16, MODE>::NTHREADS,
+                                                      Cfg<BF16, MODE>::SMEM_BYTES) != cudaSuccess)
+      return 0;
+    units = per_sm * st->sms;
+  } else {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    fill_launch<BF16, MODE>(&cfg, attr, 2 * (st->sms / 2), nullptr, false);
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, gbsdpa::attn_fwd_kernel<BF16, MODE>, &cfg) !=
+        cudaSuccess)
+      return 0;
+    units = clusters;
+  }
+  st->sk_units[idx] = std::max(0, units);
+  return st->sk_units[idx];
 }
 
 int launch_combine(const float* part_o, const float* part_ml, void* out, long long R, int D,
@@ -158,14 +219,14 @@ size_t partial_bytes(long long R, int D, int n_splits) {
 }
 
 // Kernel variant for a call: head_dim 512 splits the head dimension over a CTA
-// pair; head_dim 256 prefill uses 2-SM MMAs over 256-row query tiles, except
-// with a sliding window shorter than 4096 keys, where a 256-row tile would add
-// too many masked keys and 128-row tiles on one CTA each do less work; decode
-// uses one CTA per 16 query heads x 8 position slots.
+// pair; head_dim 256 prefill uses 2-SM MMAs over 256-row query tiles (a 2-SM
+// tile costs about two thirds of two 1-SM tiles), except with a sliding window
+// shorter than 256 keys, where most of a 256-row tile's keys would be masked;
+// decode uses one CTA per 16 query heads x 8 position slots.
 int choose_mode(bool decode, int D, int window) {
   if (D == 512) return gbsdpa::kPair;
   if (decode) return gbsdpa::kSingle;
-  return (window > 0 && window < 4096) ? gbsdpa::kSingle : gbsdpa::kDuo;
+  return (window > 0 && window < 256) ? gbsdpa::kSingle : gbsdpa::kDuo;
 }
 
 int qtile_rows(int mode) { return mode == gbsdpa::kDuo ? 256 : 128; }
@@ -219,11 +280,115 @@ int plan_decode_splits(int sms, int B, int Hq, int Hkv, int D) {
   return static_cast<int>(s);
 }
 
+// ----------------------------------------------------------- persistent plan
+// Prefill with one CTA (or 2-SM pair) per query tile leaves SMs idle when the
+// query tiles do not fill whole waves.  The persistent variant keeps one unit
+// per resident slot: units take the query tiles in waves and then share out the
+// leftover partial wave by key tiles (the schedule is spelled out beside the
+// kernel's iterator).  Only the unit count is chosen here.
+
+// Key tiles a query tile of `rows` rows starting at q0 visits (the kernel's
+// item_tiles_for_qt).
+long long qtile_key_tiles(int q0, int rows, int Lq, int Lk, int causal, int window, int bn) {
+  const int qlast = std::min(q0 + rows, Lq) - 1;
+  const int pmin = Lk - Lq + q0, pmax = Lk - Lq + qlast;
+  const int lo = (causal && window) ? std::max(0, pmin - window + 1) : 0;
+  const int hi = causal ? std::min(Lk, pmax + 1) : Lk;
+  return (hi + bn - 1) / bn - lo / bn;
+}
+
+long long total_key_tiles(int B, int Hq, int Lq, int Lk, int causal, int window, int bn, int rows) {
+  long long w = 0;
+  for (int q0 = 0; q0 < Lq; q0 += rows) w += qtile_key_tiles(q0, rows, Lq, Lk, causal, window, bn);
+  return w * B * Hq;
+}
+
+// Workspace of a persistent launch: per (slot, rank) 128 x 256 fp32 partial
+// rows, 128 (max, sum) pairs and one flag.
+struct SkLayout {
+  size_t o_off, ml_off, flag_off, bytes;
+};
+
+SkLayout sk_layout(long long units) {
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  SkLayout L;
+  L.o_off = 0;
+  L.ml_off = up(static_cast<size_t>(units) * 2 * 128 * 256 * sizeof(float));
+  L.flag_off = L.ml_off + up(static_cast<size_t>(units) * 2 * 128 * 2 * sizeof(float));
+  L.bytes = L.flag_off + up(static_cast<size_t>(units) * 2 * sizeof(unsigned long long));
+  return L;
+}
+
+// Prefix length L of the leftover items of a persistent launch (their first L
+// key tiles stay on one unit each, the rest is shared out), with the suffix
+// total SS and suffix unit count US.  Costs are in key tiles: a piece boundary
+// costs about kPieceCost (query reload, pipeline refill, partial write), the
+// prefix unit's merge about kMergeCost.  L balances the prefix units against
+// the suffix units, or is the longest leftover item (no split) when the split
+// would not be shorter.
+struct TailPlan {
+  int L = 0, US = 0;
+  long long SS = 0;
+};
+
+TailPlan plan_tail(long long units, int B, int Hq, int Lq, int Lk, int causal, int window, int bn,
+                   int rows) {
+  constexpr long long kPieceCost = 3, kMergeCost = 3;
+  TailPlan t;
+  const long long n_qtiles = (Lq + rows - 1) / rows;
+  const long long n_per = static_cast<long long>(B) * Hq;
+  const long long N = n_qtiles * n_per, U = units;
+  const long long r = N % U, base = N - r;
+  if (r == 0) return t;
+  auto T = [&](long long i) {  // key tiles of leftover item i
+    const long long qt = n_qtiles - 1 - (base + i) / n_per;
+    return qtile_key_tiles(static_cast<int>(qt * rows), rows, Lq, Lk, causal, window, bn);
+  };
+  long long wt = 0, tmax = 0;
+  for (long long i = 0; i < r; ++i) {
+    wt += T(i);
+    tmax = std::max(tmax, T(i));
+  }
+  long long L = (wt + kPieceCost * U - kMergeCost * (U - r) + U - 1) / U;
+  L = std::max(1ll, std::min(L, tmax));
+  long long ss = 0;
+  for (long long i = 0; i < r; ++i) ss += std::max(0ll, T(i) - L);
+  const long long us = std::min(U - r, ss);
+  bool split = ss > 0 && us > 0;
+  if (split) {
+    const long long per_suffix = (ss + us - 1) / us + kPieceCost * ((r + us - 1) / us + 1);
+    const long long cost = std::max(L + kMergeCost, per_suffix);
+    split = cost * 100 < tmax * 97;
+  }
+  if (!split) {
+    t.L = static_cast<int>(tmax);
+    return t;
+  }
+  t.L = static_cast<int>(L);
+  t.SS = ss;
+  t.US = static_cast<int>(us);
+  return t;
+}
+
+// Units for a persistent prefill launch (0: one CTA per query tile instead).
+template <bool BF16>
+long long persistent_units(DeviceState* st, int mode, int B, int Hq, int Lq, int Lk, int causal,
+                           int window) {
+  int units = 0;
+  if (mode == gbsdpa::kSingle) units = resident_units<BF16, gbsdpa::kSingle>(st);
+  else if (mode == gbsdpa::kDuo) units = resident_units<BF16, gbsdpa::kDuo>(st);
+  else return 0;
+  if (units <= 0) return 0;
+  const long long W =
+      total_key_tiles(B, Hq, Lq, Lk, causal, window, key_tile(mode), qtile_rows(mode));
+  return std::min<long long>(units, W);
+}
+
 template <bool BF16>
 int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv, int Lq,
         int Lk, int D, float scale, int causal, int window, bool decode, int n_splits,
         bool write_partial, void* workspace, cudaStream_t stream, DeviceState* st,
-        int withhold_q = 0) {
+        int withhold_q = 0, long long sk_units = 0) {
   AttnParams p;
   std::memset(&p, 0, sizeof(p));
   const int mode = choose_mode(decode, D, window);
@@ -267,7 +432,25 @@ int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, i
   p.write_partial = write_partial ? 1 : 0;
   p.withhold_q = withhold_q;
   long long items;
-  if (decode)
+  if (sk_units > 0) {
+    const SkLayout L = sk_layout(sk_units);
+    char* ws = static_cast<char*>(workspace);
+    p.persistent = 1;
+    p.n_units = static_cast<int>(sk_units);
+    const TailPlan tp = plan_tail(sk_units, B, Hq, Lq, Lk, causal, window, key_tile(mode),
+                                  qtile_rows(mode));
+    p.tail_L = tp.L;
+    p.tail_SS = tp.SS;
+    p.tail_US = tp.US;
+    p.sk_o = reinterpret_cast<float*>(ws + L.o_off);
+    p.sk_ml = reinterpret_cast<float*>(ws + L.ml_off);
+    p.sk_flag = reinterpret_cast<unsigned long long*>(ws + L.flag_off);
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      p.epoch = ++st->epoch;
+    }
+    items = sk_units;
+  } else if (decode)
     items = static_cast<long long>(B) * Hkv * n_splits * p.n_hb;
   else
     items = static_cast<long long>(B) * Hq * p.n_qtiles * n_splits;
@@ -291,7 +474,13 @@ size_t sdpa_prefill_workspace_bytes(int B, int Hq, int Hkv, int Lq, int Lk, int 
   DeviceState* st = nullptr;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lk <= 0 || Hq % Hkv) return 0;
   if (D != 256 && D != 512) return 0;
+  if (causal != 0 && causal != 1) return 0;
+  if (window < 0 || (causal && Lq > Lk)) return 0;
   if (device_state(&st)) return 0;
+  const int mode = choose_mode(false, D, causal ? window : 0);
+  const long long u = std::max(persistent_units<false>(st, mode, B, Hq, Lq, Lk, causal, window),
+                               persistent_units<true>(st, mode, B, Hq, Lq, Lk, causal, window));
+  if (u > 0) return sk_layout(u).bytes;
   const int s = plan_prefill_splits(st->sms, B, Hq, Lq, Lk, D, causal, window);
   if (s <= 1) return 0;
   return partial_bytes(static_cast<long long>(B) * Hq * Lq, D, s);
@@ -315,12 +504,20 @@ int sdpa_prefill(const void* q, const void* k, const void* v, void* out, int B, 
   DeviceState* st = nullptr;
   rc = device_state(&st);
   if (rc) return rc;
-  int s = plan_prefill_splits(st->sms, B, Hq, Lq, Lk, D, causal, window);
+  const bool bf16 = dtype == SDPA_BF16;
+  auto strm = reinterpret_cast<cudaStream_t>(stream);
+  const int mode = choose_mode(false, D, window);
+  const long long u = bf16 ? persistent_units<true>(st, mode, B, Hq, Lq, Lk, causal, window)
+                           : persistent_units<false>(st, mode, B, Hq, Lq, Lk, causal, window);
+  if (u > 0 && workspace && workspace_bytes >= sk_layout(u).bytes)
+    return bf16 ? run<true>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, false, 1,
+                            false, workspace, strm, st, 0, u)
+                : run<false>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, false, 1,
+                             false, workspace, strm, st, 0, u);
+  int s = u > 0 ? 1 : plan_prefill_splits(st->sms, B, Hq, Lq, Lk, D, causal, window);
   if (s > 1 && (!workspace ||
                 workspace_bytes < partial_bytes(static_cast<long long>(B) * Hq * Lq, D, s)))
     s = 1;
-  const bool bf16 = dtype == SDPA_BF16;
-  auto strm = reinterpret_cast<cudaStream_t>(stream);
   return bf16 ? run<true>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, false, s,
                           s > 1, workspace, strm, st)
               : run<false>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, false, s,

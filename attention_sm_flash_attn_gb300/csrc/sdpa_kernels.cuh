@@ -58,7 +58,7 @@ enum : int {
   kDevTimeoutXFull = 0x107,
   kDevTimeoutXFree = 0x108,
   kDevTimeoutDrain = 0x109,
-  kDevTimeoutPair = 0x10a,  // (unused: the row halves now meet at a named barrier)
+  kDevTimeoutPair = 0x10a,  // a prefix unit waited too long for a suffix piece's partials
   kDevMisaligned = 0x10b,
 };
 
@@ -83,6 +83,22 @@ struct AttnParams {
   // "query tile ready" signal, so the MMA issuer's bounded wait runs out and the
   // kernel reports a device timeout instead of computing.
   int withhold_q;
+  // Persistent prefill (SINGLE and DUO variants): `n_units` resident CTAs (CTA
+  // pairs for DUO) walk the query tiles ("items") in waves, then share out the
+  // leftover partial wave so that every unit gets about the same number of key
+  // tiles.  A leftover item is cut into a prefix, finished by one unit, and a
+  // suffix that other units compute in pieces; each piece leaves fp32 partials
+  // in its slot of sk_o / sk_ml and sets its flag to `epoch`, and the prefix
+  // unit merges them in key order.
+  int persistent;
+  int n_units;
+  int tail_L;        // prefix length (key tiles) of the leftover items
+  int tail_US;       // suffix units
+  long long tail_SS; // suffix key tiles in all
+  float* sk_o;                 // [n_units][2][128][256]  (slot, rank, row, column)
+  float* sk_ml;                // [n_units][2][128][2]
+  unsigned long long* sk_flag; // [n_units][2]
+  unsigned long long epoch;
 };
 
 // Kernel variants.
@@ -123,9 +139,18 @@ struct Cfg {
   static constexpr int XS_OFF = X_OFF + X_BYTES;     // own partial scores (staged to send)
   static constexpr int BAR_OFF = XS_OFF + X_BYTES;
   static constexpr int RED_OFF = BAR_OFF + 256;      // [2 parity][2 half][128 rows] floats
-  static constexpr int SMEM_BYTES = RED_OFF + 2048;
+  // Piece iterators: softmax warps (state + 2 pieces), producer and MMA issuer
+  // (state + 1 piece each), 256 bytes apiece.
+  static constexpr int ITER_OFF = RED_OFF + 2048;
+  static constexpr int SMEM_BYTES = ITER_OFF + 768;
   static constexpr int S_COL = 256;  // TMEM: O in columns [0,256), S buffers after it
-  static constexpr int NTHREADS = 320;  // warps 0-7 softmax, 8 producer, 9 MMA
+  // warps 0-7 softmax (warpgroups 0, 1), 8 producer, 9 MMA, 10-11 idle (warpgroup 2)
+  static constexpr int NTHREADS = 384;
+  // Registers a thread after the split; the sum stays within the launch
+  // allotment of NTHREADS x 168 (the cap for 12 warps on 4 sub-partitions).
+  static constexpr int kRegsSoftmax = 208;
+  static constexpr int kRegsOther = 88;
+  static_assert(256 * kRegsSoftmax + 128 * kRegsOther <= NTHREADS * 168, "register split");
   static constexpr int kProducerWarp = 8;
   static constexpr int kMmaWarp = 9;
   static constexpr int MMA_M = DUO ? 256 : 128;
@@ -145,6 +170,8 @@ enum {
   kBarKvFull = 1,    // + slot (8 slots max)
   kBarKvEmpty = 9,   // + slot
   kBarSFull = 17,    // + buf
+  kBarQFree = 19,    // the last S of a piece has completed: Q may be reloaded
+  kBarOFree = 20,    // the epilogue has read O: the next piece may overwrite it
   kBarPFull = 21,
   kBarPvDone = 22,
   kBarXFull = 23,
@@ -239,6 +266,184 @@ __device__ __forceinline__ Work make_work(const AttnParams& p, int item, int ran
   return w;
 }
 
+// ------------------------------------------------------------ persistent schedule
+// Items are the query tiles in make_work's order (longest causal tiles first,
+// then batch, kv head and query head within its group).  With N items and U
+// units, the first floor(N / U) * U items go out in whole waves, unit u taking
+// item u of even waves and item U - 1 - u of odd ones (concurrent units work on
+// neighbouring items, which share K/V rows in L2).  Of the r = N mod U leftover
+// items, item i keeps its first min(T_i, L) key tiles on unit i; the remaining
+// S_i = max(0, T_i - L) tiles of all of them are laid end to end and cut into
+// equal contiguous shares for units r .. r + US - 1 (the host picks L, and
+// passes US and the sum of S_i).  A suffix piece of item i on suffix unit k
+// (counted from r) writes slot i + k, which is unique because i and k never both
+// stay the same between two consecutive pieces.  Suffix units never wait, so
+// the prefix units' waits end.
+
+// Key tiles of a query tile (the same count make_work visits).
+template <int BN, int QROWS>
+__device__ __forceinline__ int item_tiles_for_qt(const AttnParams& p, int qt) {
+  const int q0 = qt * QROWS;
+  const int qlast = min(q0 + QROWS, p.Lq) - 1;
+  const int pmin = p.Lk - p.Lq + q0, pmax = p.Lk - p.Lq + qlast;
+  const int lo = (p.causal && p.window) ? max(0, pmin - p.window + 1) : 0;
+  const int hi = p.causal ? min(p.Lk, pmax + 1) : p.Lk;
+  return (hi + BN - 1) / BN - lo / BN;
+}
+
+template <int BN, int QROWS>
+__device__ __forceinline__ int item_tiles(const AttnParams& p, int idx) {
+  return item_tiles_for_qt<BN, QROWS>(p, p.n_qtiles - 1 - idx / (p.G * p.Hkv * p.B));
+}
+
+// Work of item `idx`, key tiles [t0, t0 + cnt) of its visible range.
+template <int BN, int QROWS>
+__device__ __forceinline__ Work item_work(const AttnParams& p, int idx, int rank, int t0,
+                                          int cnt) {
+  Work w;
+  int item = idx;
+  const int hl = item % p.G;
+  item /= p.G;
+  w.split = 0;
+  w.hkv = item % p.Hkv;
+  item /= p.Hkv;
+  w.b = item % p.B;
+  item /= p.B;
+  const int qt = p.n_qtiles - 1 - item;
+  w.h0 = w.hkv * p.G + hl;
+  const int q0 = qt * QROWS;
+  w.m0 = q0 + (QROWS == 256 ? rank * 128 : 0);
+  const int qlast = min(q0 + QROWS, p.Lq) - 1;
+  w.pmin = p.Lk - p.Lq + q0;
+  w.pmax = p.Lk - p.Lq + qlast;
+  const int lo = (p.causal && p.window) ? max(0, w.pmin - p.window + 1) : 0;
+  w.t_begin = lo / BN + t0;
+  w.t_step = 1;
+  w.t_count = cnt;
+  return w;
+}
+
+struct Piece {
+  Work w;
+  int kind;       // 0 whole item, 1 prefix (merges suffix slots), 2 suffix piece, 3 split partial
+  int slot;       // kind 1: first suffix slot; kind 2: own slot
+  int n_contrib;  // kind 1: suffix slots slot .. slot + n_contrib - 1, in key order
+  int valid;      // 0 once the iterator is exhausted
+};
+
+// Position of one CTA in its sequence of pieces (plain data, so the softmax
+// warps can keep it in shared memory).
+struct IterState {
+  long long pos, end;  // suffix unit: next suffix coordinate, end of its share
+  long long A;         // suffix coordinate of leftover item i's first suffix tile
+  long long L;         // prefix length of the leftover items
+  long long SS;        // suffix tiles in all
+  int stage;           // 0 waves, 1 leftover prefix, 2 suffix share, 3 done, 4 single piece
+  int w, i;            // next wave; current leftover item
+  int unit, rank;
+  int n_full, r, US;
+};
+
+template <int BN, int QROWS>
+__device__ __forceinline__ void iter_init(const AttnParams& p, IterState& st, int unit, int rank) {
+  st.unit = unit;
+  st.rank = rank;
+  st.w = 0;
+  st.i = 0;
+  st.pos = st.end = st.A = 0;
+  st.n_full = st.r = 0;
+  st.L = p.tail_L;
+  st.SS = p.tail_SS;
+  st.US = p.tail_US;
+  if (!p.persistent) {
+    st.stage = 4;
+    return;
+  }
+  const int N = p.n_qtiles * p.G * p.Hkv * p.B;
+  const int U = p.n_units;
+  st.n_full = N / U;
+  st.r = N - st.n_full * U;
+  st.stage = st.n_full > 0 ? 0 : 1;
+  if (unit >= st.r) {
+    const int k = unit - st.r;
+    if (k < st.US) {
+      st.pos = st.SS * k / st.US;
+      st.end = st.SS * (k + 1) / st.US;
+    }
+  }
+}
+
+template <int BN, int QROWS>
+__device__ __forceinline__ bool iter_next(const AttnParams& p, IterState& st, Piece& pc) {
+  pc.valid = 0;
+  pc.slot = 0;
+  pc.n_contrib = 0;
+  if (st.stage == 4) {  // one launch-planned piece per CTA
+    st.stage = 3;
+    pc.w = make_work<BN, QROWS>(p, st.unit, st.rank);
+    pc.kind = p.write_partial ? 3 : 0;
+    pc.valid = 1;
+    return true;
+  }
+  const int U = p.n_units;
+  if (st.stage == 0) {
+    const int idx = st.w * U + ((st.w & 1) ? U - 1 - st.unit : st.unit);
+    pc.w = item_work<BN, QROWS>(p, idx, st.rank, 0, item_tiles<BN, QROWS>(p, idx));
+    pc.kind = 0;
+    pc.valid = 1;
+    if (++st.w == st.n_full) st.stage = 1;
+    return true;
+  }
+  const int base = st.n_full * U;
+  if (st.stage == 1) {
+    if (st.unit < st.r) {
+      // Prefix of leftover item `unit`; its suffix, if any, is on the suffix
+      // units whose shares meet [A, A + S).
+      st.stage = 3;
+      const int i = st.unit;
+      const int T = item_tiles<BN, QROWS>(p, base + i);
+      const long long P = min(static_cast<long long>(T), st.L);
+      const long long S = T - P;
+      pc.w = item_work<BN, QROWS>(p, base + i, st.rank, 0, static_cast<int>(P));
+      pc.kind = 0;
+      if (S > 0) {
+        long long A = 0;
+        for (int j = 0; j < i; ++j) A += max(0ll, item_tiles<BN, QROWS>(p, base + j) - st.L);
+        // suffix unit holding coordinate x: the largest k with SS * k / US <= x
+        const long long kf = ((A + 1) * st.US - 1) / st.SS;
+        const long long kl = ((A + S) * st.US - 1) / st.SS;
+        pc.kind = 1;
+        pc.slot = i + static_cast<int>(kf);
+        pc.n_contrib = static_cast<int>(kl - kf + 1);
+      }
+      pc.valid = 1;
+      return true;
+    }
+    st.stage = 2;
+  }
+  if (st.stage == 2) {
+    if (st.pos >= st.end) {
+      st.stage = 3;
+      return false;
+    }
+    long long S = max(0ll, item_tiles<BN, QROWS>(p, base + st.i) - st.L);
+    while (st.A + S <= st.pos) {
+      st.A += S;
+      ++st.i;
+      S = max(0ll, item_tiles<BN, QROWS>(p, base + st.i) - st.L);
+    }
+    const long long stop = min(st.end, st.A + S);
+    const int t0 = static_cast<int>(st.L + (st.pos - st.A));
+    pc.w = item_work<BN, QROWS>(p, base + st.i, st.rank, t0, static_cast<int>(stop - st.pos));
+    pc.kind = 2;
+    pc.slot = st.i + (st.unit - st.r);
+    pc.valid = 1;
+    st.pos = stop;
+    return true;
+  }
+  return false;
+}
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
   if (bf16) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -250,7 +455,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
 }
 
 template <bool BF16, int MODE>
-__global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
   using C = Cfg<BF16, MODE>;
   constexpr bool PAIR = C::PAIR;
   constexpr bool DUO = C::DUO;
@@ -280,8 +485,9 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
   const int lane = threadIdx.x % 32;
   const uint32_t rank = CLUSTER ? ptx::cluster_ctarank() : 0u;
   const uint32_t peer = rank ^ 1u;
+  // Item (one query tile, or one split of it) or, in persistent mode, unit index.
   const int item = CLUSTER ? static_cast<int>(blockIdx.x / 2) : static_cast<int>(blockIdx.x);
-  const Work w = make_work<BN, DUO ? 256 : 128>(p, item, static_cast<int>(rank));
+  constexpr int QROWS = DUO ? 256 : 128;
   const int d0 = PAIR ? static_cast<int>(rank) * C::DH : 0;  // head-dim offset of this CTA
   // DUO: the pair's even CTA issues the MMAs and owns the barriers they wait on.
   auto leader_bar = [&](int i) -> uint32_t {
@@ -297,6 +503,8 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
     for (int b = 0; b < 2; ++b) ptx::mbar_init(bar(kBarSFull + b), 1);
     ptx::mbar_init(bar(kBarPFull), C::kPFullArrivals);
     ptx::mbar_init(bar(kBarPvDone), 1);
+    ptx::mbar_init(bar(kBarQFree), 1);
+    ptx::mbar_init(bar(kBarOFree), C::kPFullArrivals);
     ptx::mbar_init(bar(kBarXFull), 1);  // local expect_tx arrive + the peer's bulk-copy bytes
     ptx::mbar_init(bar(kBarXFree), 8);  // one arrive per softmax warp of the peer
     ptx::mbar_init(bar(kBarDrain), 1);
@@ -322,19 +530,21 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
   if (CLUSTER) ptx::cluster_sync();  // peer barriers initialised before any remote use
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int count = w.t_count;
   const bool mma_cta = !DUO || rank == 0;  // this CTA issues MMAs
 
   // Producer / MMA bookkeeping kept for the drain after an abort.
-  int issued_q = 0;
+  int issued_q = 0;  // query tiles loaded (one per piece with key tiles)
   uint32_t ring_issued = 0;  // ring loads issued, in sequence order
   int mma_issued = 0;
 
+  // Warpgroup 2 (producer, MMA issuer, two idle warps) hands its spare
+  // registers to the softmax warpgroups; each side changes its budget inside its
+  // own branch, so the code after a change is that side's alone.
+  if (warp >= 8) {
+  ptx::setmaxnreg_dec<C::kRegsOther>();
   if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && count > 0) {
-      const int bh_q = w.b * p.Hq + w.h0;
-      const int bh_kv = w.b * p.Hkv + w.hkv;
+    if (lane == 0) {
       auto load = [&](uint32_t dst, const CUtensorMap* m, uint32_t fullbar, int c0, int c1,
                       int c2) {
         if constexpr (DUO)
@@ -342,70 +552,92 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
         else
           ptx::tma_load_3d(dst, m, fullbar, c0, c1, c2);
       };
-      if (!p.decode && !p.withhold_q) {
-        const uint32_t qbar = leader_bar(kBarQ);
-        if (mma_cta) ptx::mbar_arrive_expect_tx(bar(kBarQ), DUO ? 2 * 65536 : 65536);
-        for (int c = 0; c < 4; ++c) load(sQ + c * 16384, &p.tm_q, qbar, d0 + c * 64, w.m0, bh_q);
-        issued_q = 1;
-      }
-      uint32_t n = 0;  // ring sequence number
+      uint32_t n = 0;  // ring sequence number, continued across pieces
       bool ok = true;
-      auto next_slot = [&](int& slot, uint32_t& fullbar) -> bool {
-        slot = n % C::NSLOT;
-        if (!wait_bar(bar(kBarKvEmpty + slot), ((n / C::NSLOT) & 1) ^ 1, abort_flag, p.status,
-                      kDevTimeoutKvEmpty))
-          return false;
-        fullbar = leader_bar(kBarKvFull + slot);
-        // The MMA CTA posts the bytes of both halves (DUO) on its own barrier.
-        if (mma_cta) ptx::mbar_arrive_expect_tx(bar(kBarKvFull + slot), DUO ? 2 * C::SLOT : C::SLOT);
-        return true;
-      };
-      auto load_k = [&](int j) {
-        // DUO: CTA `rank` loads keys [64 rank, 64 rank + 64) of the 128-key tile.
-        const int key0 = (w.t_begin + j * w.t_step) * BN + (DUO ? static_cast<int>(rank) * 64 : 0);
-        for (int ks = 0; ks < C::KSUB && ok; ++ks, ++n) {
-          int slot;
-          uint32_t fb;
-          if (!next_slot(slot, fb)) {
+      // Iterator in shared memory: it stays out of this warpgroup's small
+      // register budget.
+      IterState& ist = *reinterpret_cast<IterState*>(smem + C::ITER_OFF + 256);
+      Piece& pc = *reinterpret_cast<Piece*>(smem + C::ITER_OFF + 256 + 96);
+      iter_init<BN, QROWS>(p, ist, item, static_cast<int>(rank));
+      while (ok && iter_next<BN, QROWS>(p, ist, pc)) {
+        const Work& w = pc.w;
+        const int count = w.t_count;
+        if (count == 0) continue;
+        const int bh_q = w.b * p.Hq + w.h0;
+        const int bh_kv = w.b * p.Hkv + w.hkv;
+        if (!p.decode && !p.withhold_q) {
+          // The query buffer is free once the previous piece's last S has completed.
+          if (issued_q > 0 && !wait_bar(bar(kBarQFree), (issued_q - 1) & 1, abort_flag, p.status,
+                                        kDevTimeoutQ)) {
             ok = false;
             break;
           }
-          for (int e = 0; e < C::KBOX; ++e)
-            load(sRing + slot * C::SLOT + e * (C::KROWS * 128), &p.tm_k, fb,
-                 d0 + (ks * C::KBOX + e) * 64, key0, bh_kv);
-          ring_issued = n + 1;
+          const uint32_t qbar = leader_bar(kBarQ);
+          if (mma_cta) ptx::mbar_arrive_expect_tx(bar(kBarQ), DUO ? 2 * 65536 : 65536);
+          for (int c = 0; c < 4; ++c)
+            load(sQ + c * 16384, &p.tm_q, qbar, d0 + c * 64, w.m0, bh_q);
+          ++issued_q;
         }
-      };
-      auto load_v = [&](int j) {
-        // DUO: CTA `rank` loads head-dim columns [128 rank, 128 rank + 128) of V.
-        const int key0 = (w.t_begin + j * w.t_step) * BN;
-        const int dv0 = DUO ? static_cast<int>(rank) * 128 : d0;
-        for (int vs = 0; vs < C::VSUB && ok; ++vs, ++n) {
-          int slot;
-          uint32_t fb;
-          if (!next_slot(slot, fb)) {
-            ok = false;
-            break;
+        auto next_slot = [&](int& slot, uint32_t& fullbar) -> bool {
+          slot = n % C::NSLOT;
+          if (!wait_bar(bar(kBarKvEmpty + slot), ((n / C::NSLOT) & 1) ^ 1, abort_flag, p.status,
+                        kDevTimeoutKvEmpty))
+            return false;
+          fullbar = leader_bar(kBarKvFull + slot);
+          // The MMA CTA posts the bytes of both halves (DUO) on its own barrier.
+          if (mma_cta)
+            ptx::mbar_arrive_expect_tx(bar(kBarKvFull + slot), DUO ? 2 * C::SLOT : C::SLOT);
+          return true;
+        };
+        auto load_k = [&](int j) {
+          // DUO: CTA `rank` loads keys [64 rank, 64 rank + 64) of the 128-key tile.
+          const int key0 =
+              (w.t_begin + j * w.t_step) * BN + (DUO ? static_cast<int>(rank) * 64 : 0);
+          for (int ks = 0; ks < C::KSUB && ok; ++ks, ++n) {
+            int slot;
+            uint32_t fb;
+            if (!next_slot(slot, fb)) {
+              ok = false;
+              break;
+            }
+            for (int e = 0; e < C::KBOX; ++e)
+              load(sRing + slot * C::SLOT + e * (C::KROWS * 128), &p.tm_k, fb,
+                   d0 + (ks * C::KBOX + e) * 64, key0, bh_kv);
+            ring_issued = n + 1;
           }
-          for (int c = 0; c < C::VBOX; ++c)
-            load(sRing + slot * C::SLOT + c * C::V_LBO, &p.tm_v, fb, dv0 + c * 64,
-                 key0 + vs * C::VROWS, bh_kv);
-          ring_issued = n + 1;
+        };
+        auto load_v = [&](int j) {
+          // DUO: CTA `rank` loads head-dim columns [128 rank, 128 rank + 128) of V.
+          const int key0 = (w.t_begin + j * w.t_step) * BN;
+          const int dv0 = DUO ? static_cast<int>(rank) * 128 : d0;
+          for (int vs = 0; vs < C::VSUB && ok; ++vs, ++n) {
+            int slot;
+            uint32_t fb;
+            if (!next_slot(slot, fb)) {
+              ok = false;
+              break;
+            }
+            for (int c = 0; c < C::VBOX; ++c)
+              load(sRing + slot * C::SLOT + c * C::V_LBO, &p.tm_v, fb, dv0 + c * 64,
+                   key0 + vs * C::VROWS, bh_kv);
+            ring_issued = n + 1;
+          }
+        };
+        load_k(0);
+        for (int j = 1; j < count && ok; ++j) {
+          load_k(j);
+          load_v(j - 1);
         }
-      };
-      load_k(0);
-      for (int j = 1; j < count && ok; ++j) {
-        load_k(j);
-        load_v(j - 1);
+        if (ok) load_v(count - 1);
       }
-      if (ok) load_v(count - 1);
     }
   } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && count > 0 && mma_cta) {
-      bool ok = wait_bar(bar(kBarQ), 0, abort_flag, p.status, kDevTimeoutQ);
-      ptx::tc_fence_after();
-      uint32_t n = 0;
+    if (lane == 0 && mma_cta) {
+      bool ok = true;
+      uint32_t n = 0;   // ring sequence number, continued across pieces
+      int g0 = 0;       // global index of the piece's first key tile (barrier phases)
+      int done_pieces = 0;
       auto mma = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
         if constexpr (DUO)
           ptx::mma_f16_ss_pair(d, a, b, idesc, acc);
@@ -431,11 +663,10 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
         commit(kBarKvEmpty + static_cast<int>(n % C::NSLOT));
         ++n;
       };
-      auto do_s = [&](int j) {
-        // S buffer j % 2 last held S_{j-2}; the softmax read it before it
-        // produced P_{j-2}, and do_pv(j - 2) has already waited for P_{j-2}.
-        const int buf = j & 1;
-        const uint32_t d_tmem = tmem + C::S_COL + buf * BN;
+      auto do_s = [&](int gt) {
+        // S buffer gt % 2 last held S_{gt-2}; the softmax read it before it
+        // produced P_{gt-2}, and the P.V of tile gt - 2 has already waited for it.
+        const uint32_t d_tmem = tmem + C::S_COL + (gt & 1) * BN;
         for (int ks = 0; ks < C::KSUB; ++ks) {
           uint32_t sk;
           if (!consume(sk)) {
@@ -456,12 +687,21 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
           release();
           ++mma_issued;
         }
-        commit(kBarSFull + buf);
+        commit(kBarSFull + (gt & 1));
       };
-      auto do_pv = [&](int j) {
-        if (!wait_bar<DUO>(bar(kBarPFull), j & 1, abort_flag, p.status, kDevTimeoutPFull)) {
+      auto do_pv = [&](int gt, int j) {  // j: tile index within the piece
+        if (!wait_bar<DUO>(bar(kBarPFull), gt & 1, abort_flag, p.status, kDevTimeoutPFull)) {
           ok = false;
           return;
+        }
+        if (j == 0 && done_pieces > 0) {
+          // The first product of a piece overwrites O: the previous piece's
+          // epilogue must have read it.
+          if (!wait_bar<DUO>(bar(kBarOFree), (done_pieces - 1) & 1, abort_flag, p.status,
+                             kDevTimeoutPvDone)) {
+            ok = false;
+            return;
+          }
         }
         ptx::tc_fence_after();
         for (int vs = 0; vs < C::VSUB; ++vs) {
@@ -483,14 +723,32 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
         }
         commit(kBarPvDone);
       };
-      if (ok) do_s(0);
-      for (int j = 1; j < count && ok; ++j) {
-        do_s(j);
-        if (ok) do_pv(j - 1);
+      IterState& ist = *reinterpret_cast<IterState*>(smem + C::ITER_OFF + 512);
+      Piece& pc = *reinterpret_cast<Piece*>(smem + C::ITER_OFF + 512 + 96);
+      iter_init<BN, QROWS>(p, ist, item, static_cast<int>(rank));
+      while (ok && iter_next<BN, QROWS>(p, ist, pc)) {
+        const int count = pc.w.t_count;
+        if (count == 0) continue;
+        if (!wait_bar(bar(kBarQ), done_pieces & 1, abort_flag, p.status, kDevTimeoutQ)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        do_s(g0);
+        if (ok && count == 1) commit(kBarQFree);
+        for (int j = 1; j < count && ok; ++j) {
+          do_s(g0 + j);
+          if (ok && j == count - 1) commit(kBarQFree);
+          if (ok) do_pv(g0 + j - 1, j - 1);
+        }
+        if (ok) do_pv(g0 + count - 1, count - 1);
+        g0 += count;
+        ++done_pieces;
       }
-      if (ok) do_pv(count - 1);
     }
+  }
   } else {
+    ptx::setmaxnreg_inc<C::kRegsSoftmax>();
     // ------------------------------------------------------------ softmax / epilogue
     // Two threads per row: warps q and q+4 read TMEM lanes [32q, 32q+32); `half`
     // selects which half of the key columns (and of the O columns) a thread owns.
@@ -498,63 +756,27 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
     const int half = warp >> 2;
     const int t = q4 * 32 + lane;  // row of the tile == TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
-    int row_p;            // bottom-right position of this row
-    bool row_valid;
-    long long row_id;     // flat (b, h, i) row index, -1 if none
-    if (!p.decode) {
-      const int i = w.m0 + t;
-      row_valid = i < p.Lq;
-      row_p = p.Lk - p.Lq + min(i, p.Lq - 1);
-      row_id = row_valid ? (static_cast<long long>(w.b) * p.Hq + w.h0) * p.Lq + i : -1;
-    } else {
-      const int hl = t >> 3;
-      const int slot = t & 7;
-      const int base = p.Lk - p.Lq;
-      const int i = (((slot - base) % 8) + 8) % 8;
-      const int h = w.h0 + hl;
-      row_valid = (i < p.Lq) && (hl < min(p.G, 16)) && (h < (w.hkv + 1) * p.G);
-      row_p = base + (row_valid ? i : 0);
-      row_id = row_valid ? (static_cast<long long>(w.b) * p.Hq + h) * p.Lq + i : -1;
-      if (count > 0) {
-        // Decode: stage this thread's half of the row's query slice into the
-        // swizzled Q tile (16-byte chunks of 8 elements).
-        const uint4* src = reinterpret_cast<const uint4*>(p.q + row_id * p.D + d0);
-        for (int c = half * (C::DH / 16); c < (half + 1) * (C::DH / 16); ++c) {
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (row_valid) v = src[c];
-          const int dc = c >> 3, cc = c & 7;
-          const uint32_t addr = sQ + dc * 16384 + t * 128 + ((cc ^ (t & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x),
-                       "r"(v.y), "r"(v.z), "r"(v.w)
-                       : "memory");
-        }
-        ptx::fence_proxy_async_smem();
-        asm volatile("bar.sync 1, 256;" ::: "memory");
-        if (threadIdx.x == 0 && !p.withhold_q) ptx::mbar_arrive(bar(kBarQ));
-      }
-    }
-    // Per-warp arrival telling the MMA issuer that this warp's P rows are in
-    // shared memory.  In the odd CTA of a 2-SM pair the barrier is the even
-    // CTA's; the P rows stay in this CTA and are read by this SM's tensor core
-    // (the fence.proxy.async before the arrive makes them visible to it), so a
-    // CTA-scope release suffices and avoids the cost of a cluster-scope one.
-    auto warp_arrive_p = [&]() {
+    // Per-warp arrival on a barrier the MMA issuer waits on.  In the odd CTA of
+    // a 2-SM pair the barrier is the even CTA's: for P-ready, the P rows stay in
+    // this CTA and are read by this SM's tensor core (the fence.proxy.async
+    // before the arrive makes them visible to it); for O-free, this CTA's reads
+    // of its own tensor memory have completed.  A CTA-scope release suffices.
+    auto warp_arrive = [&](int barid) {
       __syncwarp();
       if (lane == 0) {
         if (DUO && rank != 0)
-          ptx::mbar_arrive_remote_cta(ptx::mapa(bar(kBarPFull), 0));
+          ptx::mbar_arrive_remote_cta(ptx::mapa(bar(barid), 0));
         else
-          ptx::mbar_arrive(bar(kBarPFull));
+          ptx::mbar_arrive(bar(barid));
       }
     };
 
     const float c = p.c;
-    float m_run = -INFINITY;  // running max of c * s (lazy: the true max may exceed it by < 8)
-    float l = 0.f;            // this half's share of the row sum
     bool ok = true;      // false once the two halves of this row pair agree to stop
     bool alive = true;   // false once a wait of this warp gave up
     int use = 0;  // pair-barrier uses so far
     const uint32_t pair_id = 2 + q4;  // named barrier of warps q4 and q4 + 4
+    int g0 = 0;   // global index of the piece's first key tile (barrier phases)
 
     // Swap one float per row with the other half of the row.  The named barrier
     // also ANDs `alive` across the 64 threads, so both warps of a pair always
@@ -568,186 +790,254 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
       return both;
     };
 
-    for (int j = 0; j < count; ++j) {
-      const int tile = w.t_begin + j * w.t_step;
-      const int kb = tile * BN + half * HB;  // first key of this thread's columns
-      const int buf = j & 1;
-      float s[HB];
-#pragma unroll
-      for (int e = 0; e < HB; ++e) s[e] = -INFINITY;
-      if (alive)
-        alive = __all_sync(0xffffffffu, wait_bar(bar(kBarSFull + buf), (j >> 1) & 1, abort_flag,
-                                                 p.status, kDevTimeoutSFull));
-      if (alive) {
-        ptx::tc_fence_after();
-        uint32_t r[HB / 32][32];
-#pragma unroll
-        for (int cch = 0; cch < HB / 32; ++cch)
-          ptx::tmem_ld32(lane_base + C::S_COL + buf * BN + half * HB + cch * 32, r[cch]);
-        ptx::tmem_wait_ld();
-#pragma unroll
-        for (int cch = 0; cch < HB / 32; ++cch) {
-          ptx::reg_fence(r[cch]);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) s[cch * 32 + e] = __uint_as_float(r[cch][e]);
-        }
-      }
-
-      if constexpr (PAIR) {
-        // Swap partial scores with the peer CTA (same rows and columns) and add
-        // them.  Each warp stages its 32 rows x HB columns (4 KB) in XS and one
-        // lane bulk-copies the block into the peer's X, completing the bytes on
-        // the peer's XFull barrier; one local arrive per tile posts the expected
-        // byte count for the block the peer sends us.
-        const uint32_t wofs = static_cast<uint32_t>(warp) * (32 * HB * 4);
-        const uint32_t rofs = wofs + static_cast<uint32_t>(lane) * (HB * 4);
-        if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(bar(kBarXFull), C::X_BYTES);
-        if (alive)  // our previous block has been received and read by the peer
-          alive = __all_sync(0xffffffffu, wait_bar<true>(bar(kBarXFree), (j & 1) ^ 1,
-                                                         abort_flag, p.status, kDevTimeoutXFree));
-        if (alive) {
-#pragma unroll
-          for (int g = 0; g < HB / 4; ++g) {
-            const uint32_t off = rofs + ((g ^ (lane & (HB / 4 - 1))) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + C::XS_OFF + off),
-                         "r"(__float_as_uint(s[4 * g])), "r"(__float_as_uint(s[4 * g + 1])),
-                         "r"(__float_as_uint(s[4 * g + 2])), "r"(__float_as_uint(s[4 * g + 3]))
+    // The piece iterator lives in shared memory: thread 0 advances it, and every
+    // piece starts at a named barrier over all 256 softmax threads that also
+    // ANDs their `ok`, so all of them agree whether to go on.
+    IterState* ist = reinterpret_cast<IterState*>(smem + C::ITER_OFF);
+    static_assert(sizeof(IterState) <= 96 && 96 + 2 * sizeof(Piece) <= 256,
+                  "iterator area holds the state and two pieces");
+    Piece* pcs = reinterpret_cast<Piece*>(smem + C::ITER_OFF + 96);  // two, by piece parity
+    const int unit = item;
+    if (threadIdx.x == 0) iter_init<BN, QROWS>(p, *ist, unit, static_cast<int>(rank));
+    for (int np = 0;; ++np) {
+      if (threadIdx.x == 0) iter_next<BN, QROWS>(p, *ist, pcs[np & 1]);
+      if (!ptx::bar_red_and(1, 256, ok)) break;
+      const Piece& pc = pcs[np & 1];
+      if (!pc.valid) break;
+      const Work& w = pc.w;
+      const int count = w.t_count;
+      int row_p;            // bottom-right position of this row
+      bool row_valid;
+      long long row_id;     // flat (b, h, i) row index, -1 if none
+      if (!p.decode) {
+        const int i = w.m0 + t;
+        row_valid = i < p.Lq;
+        row_p = p.Lk - p.Lq + min(i, p.Lq - 1);
+        row_id = row_valid ? (static_cast<long long>(w.b) * p.Hq + w.h0) * p.Lq + i : -1;
+      } else {
+        const int hl = t >> 3;
+        const int slot = t & 7;
+        const int base = p.Lk - p.Lq;
+        const int i = (((slot - base) % 8) + 8) % 8;
+        const int h = w.h0 + hl;
+        row_valid = (i < p.Lq) && (hl < min(p.G, 16)) && (h < (w.hkv + 1) * p.G);
+        row_p = base + (row_valid ? i : 0);
+        row_id = row_valid ? (static_cast<long long>(w.b) * p.Hq + h) * p.Lq + i : -1;
+        if (count > 0) {
+          // Decode: stage this thread's half of the row's query slice into the
+          // swizzled Q tile (16-byte chunks of 8 elements).
+          const uint4* src = reinterpret_cast<const uint4*>(p.q + row_id * p.D + d0);
+          for (int cq = half * (C::DH / 16); cq < (half + 1) * (C::DH / 16); ++cq) {
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (row_valid) v = src[cq];
+            const int dc = cq >> 3, cc = cq & 7;
+            const uint32_t addr = sQ + dc * 16384 + t * 128 + ((cc ^ (t & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x),
+                         "r"(v.y), "r"(v.z), "r"(v.w)
                          : "memory");
           }
           ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0)
-            ptx::bulk_copy_to_peer(ptx::mapa(sX + wofs, peer), sbase + C::XS_OFF + wofs,
-                                   32 * HB * 4, ptx::mapa(bar(kBarXFull), peer));
-          alive = __all_sync(0xffffffffu, wait_bar<true>(bar(kBarXFull), j & 1, abort_flag,
-                                                         p.status, kDevTimeoutXFull));
+          asm volatile("bar.sync 1, 256;" ::: "memory");
+          if (threadIdx.x == 0 && !p.withhold_q) ptx::mbar_arrive(bar(kBarQ));
         }
+      }
+
+      float m_run = -INFINITY;  // running max of c * s (lazy: the true max may exceed it by < 8)
+      float l = 0.f;            // this half's share of the row sum
+      for (int j = 0; j < count; ++j) {
+        const int gt = g0 + j;
+        const int tile = w.t_begin + j * w.t_step;
+        const int kb = tile * BN + half * HB;  // first key of this thread's columns
+        const int buf = gt & 1;
+        float s[HB];
+#pragma unroll
+        for (int e = 0; e < HB; ++e) s[e] = -INFINITY;
+        if (alive)
+          alive = __all_sync(0xffffffffu, wait_bar(bar(kBarSFull + buf), (gt >> 1) & 1,
+                                                   abort_flag, p.status, kDevTimeoutSFull));
         if (alive) {
+          ptx::tc_fence_after();
+          uint32_t r[HB / 32][32];
 #pragma unroll
-          for (int g = 0; g < HB / 4; ++g) {
-            const uint32_t off = rofs + ((g ^ (lane & (HB / 4 - 1))) << 4);
-            float a0, a1, a2, a3;
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
-                         : "r"(sX + off)
-                         : "memory");
-            // rank 0 adds (own + peer), rank 1 adds (peer + own): the same two
-            // operands, so both CTAs hold bit-identical scores.
-            s[4 * g] += a0;
-            s[4 * g + 1] += a1;
-            s[4 * g + 2] += a2;
-            s[4 * g + 3] += a3;
-          }
-          // Our X block may be overwritten once this warp has read it.
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive_remote_cta(ptx::mapa(bar(kBarXFree), peer));
-        }
-      }
-
-      // Mask (only on tiles that straddle the band edge or the end of the keys).
-      const int tb = tile * BN;
-      const bool edge = (tb + BN > p.Lk) || (p.causal && tb + BN - 1 > w.pmin) ||
-                        (p.causal && p.window && tb < w.pmax - p.window + 1);
-      if (edge) {
-#pragma unroll
-        for (int e = 0; e < HB; ++e) {
-          const int kj = kb + e;
-          const bool vis = kj < p.Lk && (!p.causal || kj <= row_p) &&
-                           (!p.window || row_p - kj < p.window);
-          s[e] = vis ? s[e] : -INFINITY;
-        }
-      }
-      // Row max: tree over this half, then swap with the other half.
-      float mh;
-      {
-        float mm[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mm[k] = s[k];
-#pragma unroll
-        for (int e = 8; e < HB; ++e) mm[e & 7] = fmaxf(mm[e & 7], s[e]);
-        mh = fmaxf(fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3])),
-                   fmaxf(fmaxf(mm[4], mm[5]), fmaxf(mm[6], mm[7])));
-      }
-      float mo;
-      ok = swap_half(mh, mo);
-      if (!ok) break;  // both halves of the row stop together
-      const float xm = fmaxf(mh, mo) * c;  // c > 0, so -inf stays -inf
-      const bool grow = xm > m_run + 8.0f;
-      const float m_old = m_run;
-      const bool rescale_o = grow && (m_old != -INFINITY) && (j > 0);
-      float alpha = 1.f;
-      if (grow) {
-        alpha = ptx::ex2(m_old - xm);  // 0 when m_old == -inf
-        l *= alpha;
-        m_run = xm;
-      }
-      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-
-      // Probabilities 2^(c*s - m), partial row sum, pack to 16-bit pairs.
-      uint32_t pk[HB / 2];
-      float ls[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) ls[k] = 0.f;
-#pragma unroll
-      for (int e = 0; e < HB; e += 2) {
-        const float p0 = ptx::ex2(fmaf(s[e], c, -m_use));
-        const float p1 = ptx::ex2(fmaf(s[e + 1], c, -m_use));
-        ls[(e >> 1) & 7] += p0 + p1;
-        pk[e / 2] = pack2(p0, p1, BF16);
-      }
-      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-
-      // The P buffer and O are free once the previous P.V product has completed.
-      if (j > 0 && alive)
-        alive = __all_sync(0xffffffffu, wait_bar(bar(kBarPvDone), (j - 1) & 1, abort_flag,
-                                                 p.status, kDevTimeoutPvDone));
-      // A warp whose wait gave up skips the rest of the tile; it stops together
-      // with its partner at the next swap.
-      if (!alive) continue;
-      ptx::tc_fence_after();
-      if (__any_sync(0xffffffffu, rescale_o)) {
-        const float a = rescale_o ? alpha : 1.f;
-#pragma unroll 1
-        for (int cch = 0; cch < C::DH / 64; ++cch) {
-          const uint32_t col = half * (C::DH / 2) + cch * 32;
-          uint32_t r[32];
-          ptx::tmem_ld32(lane_base + col, r);
+          for (int cch = 0; cch < HB / 32; ++cch)
+            ptx::tmem_ld32(lane_base + C::S_COL + buf * BN + half * HB + cch * 32, r[cch]);
           ptx::tmem_wait_ld();
-          ptx::reg_fence(r);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * a);
-          ptx::tmem_st32(lane_base + col, r);
+          for (int cch = 0; cch < HB / 32; ++cch) {
+            ptx::reg_fence(r[cch]);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) s[cch * 32 + e] = __uint_as_float(r[cch][e]);
+          }
         }
-        ptx::tmem_wait_st();
-      }
-      // P row -> shared memory, K-major 128B-swizzled (64 keys per 128-byte row).
-#pragma unroll
-      for (int ch = 0; ch < HB / 8; ++ch) {
-        const int gc = half * (HB / 8) + ch;
-        const int blk = gc >> 3, cc = gc & 7;
-        const uint32_t addr = sP + blk * 16384 + t * 128 + ((cc ^ (t & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * ch]),
-                     "r"(pk[4 * ch + 1]), "r"(pk[4 * ch + 2]), "r"(pk[4 * ch + 3])
-                     : "memory");
-      }
-      ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before();
-      warp_arrive_p();
-    }
 
-    if (ok && count > 0) {
-      if (alive)
-        alive = __all_sync(0xffffffffu, wait_bar(bar(kBarPvDone), (count - 1) & 1, abort_flag,
-                                                 p.status, kDevTimeoutPvDone));
-      ptx::tc_fence_after();
-      float lo = 0.f;
-      ok = swap_half(l, lo);
-      l = half == 0 ? l + lo : lo + l;  // both halves: l_0 + l_1
-    }
-    // ---------------------------------------------------------------- epilogue
-    if (ok) {
-      if (p.write_partial) {
-        const long long R = static_cast<long long>(p.B) * p.Hq * p.Lq;
+        if constexpr (PAIR) {
+          // Swap partial scores with the peer CTA (same rows and columns) and add
+          // them.  Each warp stages its 32 rows x HB columns (4 KB) in XS and one
+          // lane bulk-copies the block into the peer's X, completing the bytes on
+          // the peer's XFull barrier; one local arrive per tile posts the expected
+          // byte count for the block the peer sends us.
+          const uint32_t wofs = static_cast<uint32_t>(warp) * (32 * HB * 4);
+          const uint32_t rofs = wofs + static_cast<uint32_t>(lane) * (HB * 4);
+          if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(bar(kBarXFull), C::X_BYTES);
+          if (alive)  // our previous block has been received and read by the peer
+            alive = __all_sync(0xffffffffu, wait_bar<true>(bar(kBarXFree), (gt & 1) ^ 1,
+                                                           abort_flag, p.status, kDevTimeoutXFree));
+          if (alive) {
+#pragma unroll
+            for (int g = 0; g < HB / 4; ++g) {
+              const uint32_t off = rofs + ((g ^ (lane & (HB / 4 - 1))) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + C::XS_OFF + off),
+                           "r"(__float_as_uint(s[4 * g])), "r"(__float_as_uint(s[4 * g + 1])),
+                           "r"(__float_as_uint(s[4 * g + 2])), "r"(__float_as_uint(s[4 * g + 3]))
+                           : "memory");
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+              ptx::bulk_copy_to_peer(ptx::mapa(sX + wofs, peer), sbase + C::XS_OFF + wofs,
+                                     32 * HB * 4, ptx::mapa(bar(kBarXFull), peer));
+            alive = __all_sync(0xffffffffu, wait_bar<true>(bar(kBarXFull), gt & 1, abort_flag,
+                                                           p.status, kDevTimeoutXFull));
+          }
+          if (alive) {
+#pragma unroll
+            for (int g = 0; g < HB / 4; ++g) {
+              const uint32_t off = rofs + ((g ^ (lane & (HB / 4 - 1))) << 4);
+              float a0, a1, a2, a3;
+              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                           : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
+                           : "r"(sX + off)
+                           : "memory");
+              // rank 0 adds (own + peer), rank 1 adds (peer + own): the same two
+              // operands, so both CTAs hold bit-identical scores.
+              s[4 * g] += a0;
+              s[4 * g + 1] += a1;
+              s[4 * g + 2] += a2;
+              s[4 * g + 3] += a3;
+            }
+            // Our X block may be overwritten once this warp has read it.
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_remote_cta(ptx::mapa(bar(kBarXFree), peer));
+          }
+        }
+
+        // Mask (only on tiles that straddle the band edge or the end of the keys).
+        const int tb = tile * BN;
+        const bool edge = (tb + BN > p.Lk) || (p.causal && tb + BN - 1 > w.pmin) ||
+                          (p.causal && p.window && tb < w.pmax - p.window + 1);
+        if (edge) {
+#pragma unroll
+          for (int e = 0; e < HB; ++e) {
+            const int kj = kb + e;
+            const bool vis = kj < p.Lk && (!p.causal || kj <= row_p) &&
+                             (!p.window || row_p - kj < p.window);
+            s[e] = vis ? s[e] : -INFINITY;
+          }
+        }
+        // Row max: tree over this half, then swap with the other half.
+        float mh;
+        {
+          float mm[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mm[k] = s[k];
+#pragma unroll
+          for (int e = 8; e < HB; ++e) mm[e & 7] = fmaxf(mm[e & 7], s[e]);
+          mh = fmaxf(fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3])),
+                     fmaxf(fmaxf(mm[4], mm[5]), fmaxf(mm[6], mm[7])));
+        }
+        float mo;
+        ok = swap_half(mh, mo);
+        if (!ok) break;  // both halves of the row stop together
+        const float xm = fmaxf(mh, mo) * c;  // c > 0, so -inf stays -inf
+        const bool grow = xm > m_run + 8.0f;
+        const float m_old = m_run;
+        const bool rescale_o = grow && (m_old != -INFINITY) && (j > 0);
+        float alpha = 1.f;
+        if (grow) {
+          alpha = ptx::ex2(m_old - xm);  // 0 when m_old == -inf
+          l *= alpha;
+          m_run = xm;
+        }
+        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+
+        // Probabilities 2^(c*s - m), partial row sum, pack to 16-bit pairs.
+        uint32_t pk[HB / 2];
+        float ls[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+#pragma unroll
+        for (int e = 0; e < HB; e += 2) {
+          const float p0 = ptx::ex2(fmaf(s[e], c, -m_use));
+          const float p1 = ptx::ex2(fmaf(s[e + 1], c, -m_use));
+          ls[(e >> 1) & 7] += p0 + p1;
+          pk[e / 2] = pack2(p0, p1, BF16);
+        }
+        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+
+        // The P buffer and O are free once the previous P.V product of this
+        // piece has completed (the previous piece's epilogue waited for its own).
+        if (j > 0 && alive)
+          alive = __all_sync(0xffffffffu, wait_bar(bar(kBarPvDone), (gt - 1) & 1, abort_flag,
+                                                   p.status, kDevTimeoutPvDone));
+        // A warp whose wait gave up skips the rest of the tile; it stops together
+        // with its partner at the next swap.
+        if (!alive) continue;
+        ptx::tc_fence_after();
+        if (__any_sync(0xffffffffu, rescale_o)) {
+          const float a = rescale_o ? alpha : 1.f;
+#pragma unroll 1
+          for (int cch = 0; cch < C::DH / 64; ++cch) {
+            const uint32_t col = half * (C::DH / 2) + cch * 32;
+            uint32_t r[32];
+            ptx::tmem_ld32(lane_base + col, r);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence(r);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * a);
+            ptx::tmem_st32(lane_base + col, r);
+          }
+          ptx::tmem_wait_st();
+        }
+        // P row -> shared memory, K-major 128B-swizzled (64 keys per 128-byte row).
+#pragma unroll
+        for (int ch = 0; ch < HB / 8; ++ch) {
+          const int gc = half * (HB / 8) + ch;
+          const int blk = gc >> 3, cc = gc & 7;
+          const uint32_t addr = sP + blk * 16384 + t * 128 + ((cc ^ (t & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * ch]),
+                       "r"(pk[4 * ch + 1]), "r"(pk[4 * ch + 2]), "r"(pk[4 * ch + 3])
+                       : "memory");
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        warp_arrive(kBarPFull);
+      }
+      if (ok && count > 0) {
+        if (alive)
+          alive = __all_sync(0xffffffffu, wait_bar(bar(kBarPvDone), (g0 + count - 1) & 1,
+                                                   abort_flag, p.status, kDevTimeoutPvDone));
+        ptx::tc_fence_after();
+        float lo = 0.f;
+        ok = swap_half(l, lo);
+        l = half == 0 ? l + lo : lo + l;  // both halves: l_0 + l_1
+      }
+      // All 256 threads take the epilogue, with its CTA-wide barriers, or none.
+      ok = ptx::bar_red_and(1, 256, ok);
+      if (!ok) break;
+      // -------------------------------------------------------------- epilogue
+      const long long R = static_cast<long long>(p.B) * p.Hq * p.Lq;
+      // Suffix slot `sl` of this CTA: (max, sum) per row, and the 256 fp32 columns
+      // as 64 groups of 4, each group stored for all 128 rows in a row, so that a
+      // warp's float4 accesses to one group cover 512 contiguous bytes.
+      auto sk_row = [&](int sl) -> long long {
+        return (static_cast<long long>(sl) * 2 + rank) * 128 + t;
+      };
+      auto sk_o4 = [&](int sl, int c4) -> float4* {
+        return reinterpret_cast<float4*>(p.sk_o) +
+               ((static_cast<long long>(sl) * 2 + rank) * 64 + c4) * 128 + t;
+      };
+      if (pc.kind == 3) {
+        // Planned split: fp32 partials merged by the combine kernel.
         if (row_valid && half == 0 && (!PAIR || rank == 0)) {
           const long long pr = static_cast<long long>(w.split) * R + row_id;
           p.part_ml[2 * pr] = m_run;
@@ -771,8 +1061,11 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
             }
           }
         }
-      } else if (count > 0) {
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+      } else if (pc.kind == 2) {
+        // Suffix piece: leave the unnormalised share for the unit that holds the
+        // query tile's prefix, then publish it.
+        const long long sr = sk_row(pc.slot);
+        if (half == 0) reinterpret_cast<float2*>(p.sk_ml)[sr] = make_float2(m_run, l);
 #pragma unroll 1
         for (int cch = 0; cch < C::DH / 64; ++cch) {
           const int col = half * (C::DH / 2) + cch * 32;
@@ -780,20 +1073,99 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
           ptx::tmem_ld32(lane_base + col, r);
           ptx::tmem_wait_ld();
           ptx::reg_fence(r);
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            *sk_o4(pc.slot, col / 4 + g) =
+                make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                            __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (threadIdx.x == 0) {
+          __threadfence();
+          asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p.sk_flag + pc.slot * 2 + rank),
+                       "l"(p.epoch)
+                       : "memory");
+        }
+      } else if (count > 0) {
+        // Whole query tile (kind 0) or prefix (kind 1): merge the suffix shares,
+        // if any, in key order, then normalise and store.
+        const int n_contrib = pc.kind == 1 ? pc.n_contrib : 0;
+        if (n_contrib > 0) {
+          if (threadIdx.x == 0) {
+            for (int k = 0; k < n_contrib; ++k) {
+              const unsigned long long* f = p.sk_flag + (pc.slot + k) * 2 + rank;
+              const uint64_t t0 = ptx::globaltimer();
+              for (uint32_t it2 = 0;; ++it2) {
+                unsigned long long v;
+                asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(f) : "memory");
+                if (v == p.epoch) break;
+                if ((it2 & 63) == 63 && (*abort_flag || ptx::globaltimer() - t0 > kTimeoutNs)) {
+                  *abort_flag = 1;
+                  atomicCAS(p.status, 0, kDevTimeoutPair);
+                  break;
+                }
+              }
+            }
+          }
+          asm volatile("bar.sync 1, 256;" ::: "memory");
+        }
+        // Combined max and sum (fixed order: own share, then units in order).
+        float mtot = m_run;
+        for (int k = 0; k < n_contrib; ++k) {
+          const float2 mlk = __ldcg(reinterpret_cast<const float2*>(p.sk_ml) + sk_row(pc.slot + k));
+          if (mlk.y > 0.f) mtot = fmaxf(mtot, mlk.x);
+        }
+        const float a_own = n_contrib == 0 ? 1.f : (l > 0.f ? ptx::ex2(m_run - mtot) : 0.f);
+        float ltot = a_own * l;
+        for (int k = 0; k < n_contrib; ++k) {
+          const float2 mlk = __ldcg(reinterpret_cast<const float2*>(p.sk_ml) + sk_row(pc.slot + k));
+          if (mlk.y > 0.f) ltot += ptx::ex2(mlk.x - mtot) * mlk.y;
+        }
+        const float inv = ltot > 0.f ? 1.f / ltot : 0.f;
+#pragma unroll 1
+        for (int cch = 0; cch < C::DH / 64; ++cch) {
+          const int col = half * (C::DH / 2) + cch * 32;
+          uint32_t r[32];
+          ptx::tmem_ld32(lane_base + col, r);
+          ptx::tmem_wait_ld();
+          ptx::reg_fence(r);
+          float o[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(r[e]) * a_own;
+          for (int k = 0; k < n_contrib; ++k) {
+            const long long sr = sk_row(pc.slot + k);
+            const float2 mlk = __ldcg(reinterpret_cast<const float2*>(p.sk_ml) + sr);
+            if (!(mlk.y > 0.f)) continue;
+            const float ak = ptx::ex2(mlk.x - mtot);
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              const float4 v = __ldcg(sk_o4(pc.slot + k, col / 4 + g));
+              o[4 * g] = fmaf(ak, v.x, o[4 * g]);
+              o[4 * g + 1] = fmaf(ak, v.y, o[4 * g + 1]);
+              o[4 * g + 2] = fmaf(ak, v.z, o[4 * g + 2]);
+              o[4 * g + 3] = fmaf(ak, v.w, o[4 * g + 3]);
+            }
+          }
           if (row_valid) {
             uint4* dst = reinterpret_cast<uint4*>(p.out + row_id * p.D + d0 + col);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
               uint4 v;
-              v.x = pack2(__uint_as_float(r[8 * g + 0]) * inv, __uint_as_float(r[8 * g + 1]) * inv, BF16);
-              v.y = pack2(__uint_as_float(r[8 * g + 2]) * inv, __uint_as_float(r[8 * g + 3]) * inv, BF16);
-              v.z = pack2(__uint_as_float(r[8 * g + 4]) * inv, __uint_as_float(r[8 * g + 5]) * inv, BF16);
-              v.w = pack2(__uint_as_float(r[8 * g + 6]) * inv, __uint_as_float(r[8 * g + 7]) * inv, BF16);
+              v.x = pack2(o[8 * g + 0] * inv, o[8 * g + 1] * inv, BF16);
+              v.y = pack2(o[8 * g + 2] * inv, o[8 * g + 3] * inv, BF16);
+              v.z = pack2(o[8 * g + 4] * inv, o[8 * g + 5] * inv, BF16);
+              v.w = pack2(o[8 * g + 6] * inv, o[8 * g + 7] * inv, BF16);
               dst[g] = v;
             }
           }
         }
       }
+      if (count > 0) {
+        // This piece's reads of O are complete: the next piece may overwrite it.
+        ptx::tc_fence_before();
+        warp_arrive(kBarOFree);
+      }
+      g0 += count;
     }
   }
 
@@ -803,7 +1175,8 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
   if (*abort_flag) {
     // Let every copy and MMA this CTA started finish before its memory goes away.
     if (warp == C::kProducerWarp && lane == 0) {
-      if (issued_q && mma_cta) wait_bar(bar(kBarQ), 0, abort_flag, p.status, kDevTimeoutDrain);
+      if (issued_q && mma_cta)
+        wait_bar(bar(kBarQ), (issued_q - 1) & 1, abort_flag, p.status, kDevTimeoutDrain);
       for (int s = 0; s < C::NSLOT; ++s)
         if (static_cast<uint32_t>(s) < ring_issued && mma_cta) {
           // the most recent load into slot s had sequence number `last`
@@ -837,6 +1210,7 @@ __global__ void __launch_bounds__(320, 1) attn_fwd_kernel(const __grid_constant_
       ptx::tmem_dealloc(tmem, 512);
   }
 }
+
 
 // Merge split partials: for each row, M = max_s m_s, l = sum_s 2^(m_s - M) l_s,
 // out = sum_s 2^(m_s - M) O_s / l, splits that saw no visible key (l_s == 0)
