@@ -17,13 +17,15 @@ import torch
 from . import build as _build
 
 __all__ = [
-    "sdpa_prefill", "sdpa_decode", "prefill_workspace_bytes", "decode_workspace_bytes",
+    "sdpa_prefill", "sdpa_decode", "prefill_workspace_bytes", "prefill_launches",
+    "decode_workspace_bytes",
     "device_status", "status_string", "library_path", "load_library", "SdpaError",
     "EXPORTED_SYMBOLS",
 ]
 
 SDPA_F16, SDPA_BF16 = 0, 1
-EXPORTED_SYMBOLS = ("sdpa_prefill", "sdpa_prefill_workspace_bytes", "sdpa_decode",
+EXPORTED_SYMBOLS = ("sdpa_prefill", "sdpa_prefill_workspace_bytes", "sdpa_prefill_launches",
+                    "sdpa_decode",
                     "sdpa_decode_workspace_bytes", "sdpa_device_status", "sdpa_status_string",
                     "sdpa_version", "sdpa_decode_noalloc", "sdpa_selftest_timeout")
 # Size of the library-resident scratch used by sdpa_decode_noalloc (see the header).
@@ -61,6 +63,8 @@ def load_library(path: str | None = None):
         lib.sdpa_decode.restype = i
         lib.sdpa_prefill_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
         lib.sdpa_prefill_workspace_bytes.restype = sz
+        lib.sdpa_prefill_launches.argtypes = [i, i, i, i, i, i, i, i, sz]
+        lib.sdpa_prefill_launches.restype = i
         lib.sdpa_decode_workspace_bytes.argtypes = [i, i, i, i, i]
         lib.sdpa_decode_workspace_bytes.restype = sz
         lib.sdpa_device_status.argtypes = [vp, ctypes.POINTER(i)]
@@ -122,6 +126,15 @@ def _check(q, k, v, out):
 def prefill_workspace_bytes(B, Hq, Hkv, Lq, Lk, D, causal=False, window=0) -> int:
     return int(load_library().sdpa_prefill_workspace_bytes(B, Hq, Hkv, Lq, Lk, D, int(causal),
                                                            int(window)))
+
+
+def prefill_launches(B, Hq, Hkv, Lq, Lk, D, causal=False, window=0, workspace_bytes=0) -> int:
+    """Kernel launches one sdpa_prefill call makes with that much workspace."""
+    n = int(load_library().sdpa_prefill_launches(B, Hq, Hkv, Lq, Lk, D, int(causal), int(window),
+                                                  int(workspace_bytes)))
+    if n < 0:
+        raise SdpaError(n, "sdpa_prefill_launches")
+    return n
 
 
 def decode_workspace_bytes(B, Hq, Hkv, Lq, D) -> int:

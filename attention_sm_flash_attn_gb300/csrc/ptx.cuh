@@ -118,6 +118,12 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   return r;
 }
 
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
 // Shared-memory address of the same variable in CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t mapa(uint32_t local, uint32_t rank) {
   uint32_t r;

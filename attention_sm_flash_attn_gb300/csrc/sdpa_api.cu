@@ -120,7 +120,7 @@ int ensure_attr(DeviceState* st) {
 
 template <bool BF16, int MODE>
 void fill_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, long long ctas,
-                 cudaStream_t stream, bool cooperative) {
+                 cudaStream_t stream) {
   constexpr bool kCluster = MODE != gbsdpa::kSingle;
   *cfg = {};
   cfg->gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
@@ -130,16 +130,11 @@ void fill_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, long long c
   cfg->attrs = attr;
   cfg->numAttrs = 0;
   if (kCluster) {
-    attr[cfg->numAttrs].id = cudaLaunchAttributeClusterDimension;
-    attr[cfg->numAttrs].val.clusterDim.x = 2;
-    attr[cfg->numAttrs].val.clusterDim.y = 1;
-    attr[cfg->numAttrs].val.clusterDim.z = 1;
-    ++cfg->numAttrs;
-  }
-  if (cooperative) {
-    attr[cfg->numAttrs].id = cudaLaunchAttributeCooperative;
-    attr[cfg->numAttrs].val.cooperative = 1;
-    ++cfg->numAttrs;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg->numAttrs = 1;
   }
 }
 
@@ -151,19 +146,13 @@ int launch_attn(const AttnParams& p, long long items, cudaStream_t stream, Devic
   const long long ctas = items * (kCluster ? 2 : 1);
   if (ctas <= 0 || ctas > 0x7fffffffll) return SDPA_ERR_INVALID_ARG;
   cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[2];
-  // A persistent grid waits on itself, so all of its CTAs must be resident at
-  // once: ask for a cooperative launch, which refuses a grid that cannot be.
-  fill_launch<BF16, MODE>(&cfg, attr, ctas, stream, p.persistent != 0);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gbsdpa::attn_fwd_kernel<BF16, MODE>, p);
-  if (e != cudaSuccess && p.persistent) {
-    // Cooperative launches of clusters may be refused.  The grid is already
-    // sized to the occupancy limit, and a unit that never became resident would
-    // only make its owner's bounded wait report a timeout.
-    (void)cudaGetLastError();
-    fill_launch<BF16, MODE>(&cfg, attr, ctas, stream, false);
-    e = cudaLaunchKernelEx(&cfg, gbsdpa::attn_fwd_kernel<BF16, MODE>, p);
-  }
+  cudaLaunchAttribute attr[1];
+  // A persistent grid waits on itself (prefix units on suffix units).  It is
+  // sized to the occupancy limit, so on an otherwise idle GPU all of it is
+  // resident; the kernel starts the never-waiting units first, and a wait that
+  // still runs out reports a device timeout instead of hanging.
+  fill_launch<BF16, MODE>(&cfg, attr, ctas, stream);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gbsdpa::attn_fwd_kernel<BF16, MODE>, p);
   return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
@@ -184,8 +173,8 @@ int resident_units(DeviceState* st) {
     units = per_sm * st->sms;
   } else {
     cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[2];
-    fill_launch<BF16, MODE>(&cfg, attr, 2 * (st->sms / 2), nullptr, false);
+    cudaLaunchAttribute attr[1];
+    fill_launch<BF16, MODE>(&cfg, attr, 2 * (st->sms / 2), nullptr);
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, gbsdpa::attn_fwd_kernel<BF16, MODE>, &cfg) !=
         cudaSuccess)
@@ -486,6 +475,24 @@ size_t sdpa_prefill_workspace_bytes(int B, int Hq, int Hkv, int Lq, int Lk, int 
   return partial_bytes(static_cast<long long>(B) * Hq * Lq, D, s);
 }
 
+int sdpa_prefill_launches(int B, int Hq, int Hkv, int Lq, int Lk, int D, int causal, int window,
+                          size_t workspace_bytes) {
+  // The same checks sdpa_prefill makes on sizes and flags (no pointers here).
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lk <= 0 || Hq % Hkv) return SDPA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return SDPA_ERR_INVALID_ARG;
+  if (window < 0 || (window > 0 && !causal) || (causal && Lq > Lk)) return SDPA_ERR_INVALID_ARG;
+  if (D != 256 && D != 512) return SDPA_ERR_UNSUPPORTED;
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  const int mode = choose_mode(false, D, window);
+  const long long u = persistent_units<false>(st, mode, B, Hq, Lq, Lk, causal, window);
+  if (u > 0) return 1;  // persistent with the workspace, one CTA per tile without
+  const int s = plan_prefill_splits(st->sms, B, Hq, Lq, Lk, D, causal, window);
+  return (s > 1 && workspace_bytes >= partial_bytes(static_cast<long long>(B) * Hq * Lq, D, s))
+             ? 2 : 1;
+}
+
 size_t sdpa_decode_workspace_bytes(int B, int Hq, int Hkv, int Lq, int D) {
   DeviceState* st = nullptr;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lq > 8 || Hq % Hkv) return 0;
@@ -572,7 +579,7 @@ const char* sdpa_status_string(int status) {
     case SDPA_ERR_UNSUPPORTED: return "unsupported head dim or dtype";
     case SDPA_ERR_WORKSPACE: return "workspace missing or too small";
     case SDPA_ERR_CUDA: return "CUDA runtime or driver call failed";
-    case SDPA_ERR_DEVICE_TIMEOUT: return "a kernel wait gave up (device timeout)";
+    case SDPA_ERR_DEVICE_TIMEOUT: return "a kernel wait gave up (device timeout) or a kernel check failed";
     case SDPA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
     case SDPA_ERR_SCRATCH_LIMIT:
       return "call needs more than the built-in scratch of sdpa_decode_noalloc";

@@ -60,6 +60,7 @@ enum : int {
   kDevTimeoutDrain = 0x109,
   kDevTimeoutPair = 0x10a,  // a prefix unit waited too long for a suffix piece's partials
   kDevMisaligned = 0x10b,
+  kDevBadCluster = 0x10c,  // a 2-CTA variant was launched without a cluster of 2
 };
 
 struct AttnParams {
@@ -480,13 +481,23 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
     if (threadIdx.x == 0) atomicCAS(p.status, 0, kDevMisaligned);
     return;
   }
+  // The 2-CTA variants address their peer's shared memory and pair their MMAs:
+  // without a cluster of two that would touch memory that is not there.
+  if (CLUSTER && ptx::cluster_nctarank() != 2) {
+    if (threadIdx.x == 0) atomicCAS(p.status, 0, kDevBadCluster);
+    return;
+  }
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const uint32_t rank = CLUSTER ? ptx::cluster_ctarank() : 0u;
   const uint32_t peer = rank ^ 1u;
   // Item (one query tile, or one split of it) or, in persistent mode, unit index.
-  const int item = CLUSTER ? static_cast<int>(blockIdx.x / 2) : static_cast<int>(blockIdx.x);
+  // Persistent units are numbered from the end of the grid: blocks start in
+  // index order, so should the grid not be resident all at once, the suffix
+  // units (the highest unit numbers, which never wait) start first.
+  const int cta_pair = CLUSTER ? static_cast<int>(blockIdx.x / 2) : static_cast<int>(blockIdx.x);
+  const int item = p.persistent ? p.n_units - 1 - cta_pair : cta_pair;
   constexpr int QROWS = DUO ? 256 : 128;
   const int d0 = PAIR ? static_cast<int>(rank) * C::DH : 0;  // head-dim offset of this CTA
   // DUO: the pair's even CTA issues the MMAs and owns the barriers they wait on.

@@ -16,6 +16,8 @@ decode in GB/s, transient device memory against kL).
 from __future__ import annotations
 
 import argparse
+import glob
+import hashlib
 import json
 import math
 import os
@@ -77,6 +79,41 @@ def peaks():
         except Exception:
             pass
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------- ncu traffic
+
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "attn_fwd_duo_longkv_gqa_prefill_hd256.txt")
+
+
+def kernel_sources_digest() -> str:
+    """sha256 over the CUDA sources and the public header, in name order."""
+    files = sorted(glob.glob(os.path.join(ROOT, "attention_sm_flash_attn_gb300", "csrc", "*.cu*"))
+                   + glob.glob(os.path.join(ROOT, "include", "*.h")))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the timed kernel from the committed ncu summary,
+    or None when that summary was taken on other kernel sources."""
+    keys = ("kernel_sources_sha256", "dram_bytes_per_launch")
+    try:
+        fields = dict(line.split(":", 1) for line in open(TRAFFIC_SUMMARY)
+                      if line.split(":", 1)[0] in keys)
+    except OSError:
+        return None
+    digest = fields.get("kernel_sources_sha256", "").strip()
+    if digest != kernel_sources_digest():
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"].strip())
+    except (KeyError, ValueError):
+        return None
 
 
 # ---------------------------------------------------------------- clocks
@@ -382,7 +419,8 @@ def main():
     out = torch.empty_like(q)
     ws_bytes = gb.prefill_workspace_bytes(w.B, w.Hq, w.Hkv, w.Lq, w.Lk, w.D, w.causal, w.window)
     ws = torch.empty(max(1, ws_bytes), dtype=torch.uint8, device=device)
-    launches_per_call = 2 if ws_bytes > 0 else 1
+    launches_per_call = gb.prefill_launches(w.B, w.Hq, w.Hkv, w.Lq, w.Lk, w.D, w.causal, w.window,
+                                            ws.numel())
     fn = lambda: gb.sdpa_prefill(q, k, v, out, scale=w.scale, causal=w.causal, window=w.window,
                                  workspace=ws)
     flush = L2Flush(device)
@@ -439,7 +477,10 @@ def main():
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": round(per_launch_tf, 2),
                      "peak": bf16_peak, "unit": "TFLOP/s",
-                     "frac": round(per_launch_tf / bf16_peak, 4), "traffic": None,
+                     "frac": round(per_launch_tf / bf16_peak, 4),
+                     "traffic": profiled_traffic() if launches_per_call == 1 else None,
+                     "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum of one "
+                                       "ncu capture of this kernel build (profiles/), per launch",
                      "peak_source": f"{peak_src} bf16 dense burst (fp16 rate taken equal)",
                      "timed": "whole sdpa_prefill call on its stream (attention kernel"
                               + (" + combine kernel)" if launches_per_call == 2 else ")")},

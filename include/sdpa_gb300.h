@@ -85,20 +85,35 @@ enum sdpa_status {
  * causal  0 or 1; causal rows are aligned bottom-right (p_i = Lk - Lq + i).
  * window  0 (none) or > 0 with causal = 1.
  * workspace / workspace_bytes: optional.  With NULL (or too small a buffer) the
- *   whole visible key range of each 128-row query tile is processed by one CTA;
- *   with at least sdpa_prefill_workspace_bytes(...) bytes, long key ranges may
- *   be split across CTAs and merged (fp32 partials), which keeps all SMs busy
- *   when Lq is much smaller than Lk.
+ *   whole visible key range of each query tile is processed by one CTA (pair),
+ *   one launch per tile in a single grid.  With at least
+ *   sdpa_prefill_workspace_bytes(...) bytes, head_dim 256 runs persistently:
+ *   one unit per resident CTA slot takes the query tiles in waves and the last,
+ *   partial wave is shared out by key tiles (fp32 partials merged in key
+ *   order inside the kernel); head_dim 512 may split long key ranges across
+ *   CTAs and merge them in a second kernel.  Either keeps all SMs busy when the
+ *   query tiles do not fill whole waves.  A workspace must not be used by two
+ *   calls that can run at the same time.
  * Returns SDPA_OK or a negative sdpa_status.
  */
 int sdpa_prefill(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
                  int Lq, int Lk, int D, float scale, int causal, int window, int dtype,
                  void* workspace, size_t workspace_bytes, sdpa_stream_t stream);
 
-/* Workspace that lets sdpa_prefill split long key ranges; 0 if it never would.
- * Bounded by 8 * B * Hq * Lq * (D + 2) * 4 bytes, independent of Lk's size. */
+/* Workspace for the persistent (head_dim 256) or split (head_dim 512) prefill
+ * schedule; 0 if the call would never use one.  It does not grow with Lk: at
+ * most (SM count) x 264 KiB for head_dim 256 (about 40 MB on a GB300), at most
+ * 8 * B * Hq * Lq * (D + 2) * 4 bytes for head_dim 512.  Returns 0 for
+ * arguments sdpa_prefill would reject. */
 size_t sdpa_prefill_workspace_bytes(int B, int Hq, int Hkv, int Lq, int Lk, int D, int causal,
                                     int window);
+
+/* Kernel launches one sdpa_prefill call makes with a workspace of
+ * `workspace_bytes` bytes (0 for none): 1 (one attention kernel) or 2 (split
+ * key ranges plus the merge kernel); a negative sdpa_status for arguments
+ * sdpa_prefill would reject.  Host-only; queues nothing. */
+int sdpa_prefill_launches(int B, int Hq, int Hkv, int Lq, int Lk, int D, int causal, int window,
+                          size_t workspace_bytes);
 
 /*
  * Decode / speculative verify: 1 <= Lq <= 8 query rows per head over Lk keys.
@@ -125,7 +140,11 @@ size_t sdpa_decode_workspace_bytes(int B, int Hq, int Hkv, int Lq, int D);
 
 /* Synchronises `stream`, returns SDPA_OK or SDPA_ERR_DEVICE_TIMEOUT for the
  * current device and clears the status word.  *detail (if not NULL) receives
- * the raw device code identifying the wait that gave up (0 if none). */
+ * the raw device code (0 if none): 0x100..0x10a identify the pipeline wait that
+ * gave up, 0x10b a shared-memory window that was not 1024-byte aligned, 0x10c a
+ * 2-CTA kernel that found itself outside a cluster of two.  In every case the
+ * kernel stopped without touching memory it should not and its output is
+ * unspecified. */
 int sdpa_device_status(sdpa_stream_t stream, int* detail);
 
 /* Human-readable text for an sdpa_status value (static storage). */

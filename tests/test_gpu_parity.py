@@ -68,8 +68,10 @@ def test_prefill_matches_oracle(case, dtype):
 
 @pytest.mark.parametrize("case", [(1, 2, 1, 128, 4100, 256, True, 0), (1, 2, 1, 64, 3000, 512, False, 0)])
 def test_prefill_without_workspace_matches_split_path(case):
-    """The same call with and without a workspace (one CTA per query tile vs
-    split key ranges merged by the combine kernel) both match the oracle."""
+    """The same call with and without a workspace both match the oracle: with
+    one, head_dim 256 runs the persistent schedule and head_dim 512 splits key
+    ranges merged by the combine kernel; without one, each query tile is one
+    CTA (pair) over its whole key range."""
     B, Hq, Hkv, Lq, Lk, D, causal, window = case
     q, k, v = draw(B, Hq, Hkv, Lq, Lk, D, torch.float16, seed=5)
     qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)

@@ -83,6 +83,13 @@ def test_workspace_queries_reject_bad_shapes(lib):
     assert lib.sdpa_prefill_workspace_bytes(1, 2, 1, 4, 8, 128, 1, 0) == 0
 
 
+def test_launch_query_rejects_bad_arguments_on_the_host(lib):
+    assert lib.sdpa_prefill_launches(1, 2, 1, 4, 8, 128, 1, 0, 0) == -2   # head dim
+    assert lib.sdpa_prefill_launches(1, 3, 2, 4, 8, 256, 1, 0, 0) == -1   # Hq % Hkv
+    assert lib.sdpa_prefill_launches(1, 2, 1, 4, 8, 256, 0, 16, 0) == -1  # window w/o causal
+    assert lib.sdpa_prefill_launches(1, 2, 1, 9, 8, 256, 1, 0, 0) == -1   # causal Lq > Lk
+
+
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError):
         gb.load_library(str(tmp_path / "nope.so"))
