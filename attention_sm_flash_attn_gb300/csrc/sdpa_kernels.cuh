@@ -853,6 +853,27 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
         }
       }
 
+      // Pair: rows of this warp whose partial scores go through the exchange.  In
+      // decode only the real query rows do (16 x Lq of the 128), packed in row
+      // order; both CTAs of the pair hold the same rows, so they agree on the
+      // packing.  `xbytes` (thread 0) is what the peer sends per tile.
+      uint32_t xmask = 0xffffffffu;
+      uint32_t xbytes = C::X_BYTES;
+      if (PAIR && p.decode) {
+        xmask = __ballot_sync(0xffffffffu, row_valid);
+        if (threadIdx.x == 0) {
+          int nv = 0;
+          for (int r = 0; r < 128; ++r) {
+            const int ri = ((((r & 7) - (p.Lk - p.Lq)) % 8) + 8) % 8;
+            nv += (ri < p.Lq) && ((r >> 3) < min(p.G, 16)) &&
+                  (w.h0 + (r >> 3) < (w.hkv + 1) * p.G);
+          }
+          xbytes = static_cast<uint32_t>(nv) * BN * 4;  // both column halves of each row
+        }
+      }
+      const uint32_t xidx = __popc(xmask & ((1u << lane) - 1u));  // packed position
+      const bool xrow = (xmask >> lane) & 1u;
+
       float m_run = -INFINITY;  // running max of c * s (lazy: the true max may exceed it by < 8)
       float l = 0.f;            // this half's share of the row sum
       for (int j = 0; j < count; ++j) {
@@ -883,37 +904,41 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
 
         if constexpr (PAIR) {
           // Swap partial scores with the peer CTA (same rows and columns) and add
-          // them.  Each warp stages its 32 rows x HB columns (4 KB) in XS and one
-          // lane bulk-copies the block into the peer's X, completing the bytes on
-          // the peer's XFull barrier; one local arrive per tile posts the expected
-          // byte count for the block the peer sends us.
+          // them.  Each warp stages its exchanged rows' HB columns (up to 4 KB) in
+          // XS and one lane bulk-copies the block into the peer's X, completing
+          // the bytes on the peer's XFull barrier; one local arrive per tile posts
+          // the expected byte count for the blocks the peer sends us.
           const uint32_t wofs = static_cast<uint32_t>(warp) * (32 * HB * 4);
-          const uint32_t rofs = wofs + static_cast<uint32_t>(lane) * (HB * 4);
-          if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(bar(kBarXFull), C::X_BYTES);
+          const uint32_t rofs = wofs + xidx * (HB * 4);
+          const uint32_t xsw = xidx & (HB / 4 - 1);  // chunk swizzle of this row
+          if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(bar(kBarXFull), xbytes);
           if (alive)  // our previous block has been received and read by the peer
             alive = __all_sync(0xffffffffu, wait_bar<true>(bar(kBarXFree), (gt & 1) ^ 1,
                                                            abort_flag, p.status, kDevTimeoutXFree));
           if (alive) {
+            if (xrow) {
 #pragma unroll
-            for (int g = 0; g < HB / 4; ++g) {
-              const uint32_t off = rofs + ((g ^ (lane & (HB / 4 - 1))) << 4);
-              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + C::XS_OFF + off),
-                           "r"(__float_as_uint(s[4 * g])), "r"(__float_as_uint(s[4 * g + 1])),
-                           "r"(__float_as_uint(s[4 * g + 2])), "r"(__float_as_uint(s[4 * g + 3]))
-                           : "memory");
+              for (int g = 0; g < HB / 4; ++g) {
+                const uint32_t off = rofs + ((g ^ xsw) << 4);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + C::XS_OFF + off),
+                             "r"(__float_as_uint(s[4 * g])), "r"(__float_as_uint(s[4 * g + 1])),
+                             "r"(__float_as_uint(s[4 * g + 2])), "r"(__float_as_uint(s[4 * g + 3]))
+                             : "memory");
+              }
             }
             ptx::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0)
+            const uint32_t nrows = __popc(xmask);
+            if (lane == 0 && nrows > 0)
               ptx::bulk_copy_to_peer(ptx::mapa(sX + wofs, peer), sbase + C::XS_OFF + wofs,
-                                     32 * HB * 4, ptx::mapa(bar(kBarXFull), peer));
+                                     nrows * HB * 4, ptx::mapa(bar(kBarXFull), peer));
             alive = __all_sync(0xffffffffu, wait_bar<true>(bar(kBarXFull), gt & 1, abort_flag,
                                                            p.status, kDevTimeoutXFull));
           }
-          if (alive) {
+          if (alive && xrow) {
 #pragma unroll
             for (int g = 0; g < HB / 4; ++g) {
-              const uint32_t off = rofs + ((g ^ (lane & (HB / 4 - 1))) << 4);
+              const uint32_t off = rofs + ((g ^ xsw) << 4);
               float a0, a1, a2, a3;
               asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                            : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
@@ -926,6 +951,8 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
               s[4 * g + 2] += a2;
               s[4 * g + 3] += a3;
             }
+          }
+          if (alive) {
             // Our X block may be overwritten once this warp has read it.
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive_remote_cta(ptx::mapa(bar(kBarXFree), peer));
