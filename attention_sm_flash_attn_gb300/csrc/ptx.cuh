@@ -12,6 +12,16 @@
 namespace gbsdpa {
 namespace ptx {
 
+// Programmatic dependent launch: let the next grid on the stream (launched with
+// programmatic stream serialization) start its CTAs, and, in that grid, wait
+// until the previous grid has completed and its memory is visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Per-warpgroup register budget (all four warps of the warpgroup execute it).
 template <int N>
 __device__ __forceinline__ void setmaxnreg_inc() {

@@ -190,14 +190,23 @@ int launch_combine(const float* part_o, const float* part_ml, void* out, long lo
   // weights (n_splits + 1, padded to 4 floats) then 8 x 32 float4 warp sums
   const size_t sh = static_cast<size_t>((n_splits + 4) & ~3) * sizeof(float) + 8 * 32 * 16;
   if (R <= 0 || R > 0x7fffffffll || D % 128 != 0) return SDPA_ERR_INVALID_ARG;
-  const dim3 grid(static_cast<unsigned>(R), static_cast<unsigned>(D / 128));
-  if (bf16)
-    gbsdpa::combine_kernel<true><<<grid, gbsdpa::kCombineThreads, sh, stream>>>(
-        part_o, part_ml, static_cast<uint16_t*>(out), R, D, n_splits);
-  else
-    gbsdpa::combine_kernel<false><<<grid, gbsdpa::kCombineThreads, sh, stream>>>(
-        part_o, part_ml, static_cast<uint16_t*>(out), R, D, n_splits);
-  return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+  // Programmatic dependent launch: the merge grid's CTAs may be placed while the
+  // attention grid drains; the kernel waits for that grid before reading.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(R), static_cast<unsigned>(D / 128));
+  cfg.blockDim = dim3(gbsdpa::kCombineThreads, 1, 1);
+  cfg.dynamicSmemBytes = sh;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  uint16_t* o = static_cast<uint16_t*>(out);
+  const cudaError_t e =
+      bf16 ? cudaLaunchKernelEx(&cfg, gbsdpa::combine_kernel<true>, part_o, part_ml, o, R, D, n_splits)
+           : cudaLaunchKernelEx(&cfg, gbsdpa::combine_kernel<false>, part_o, part_ml, o, R, D, n_splits);
+  return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
 size_t partial_bytes(long long R, int D, int n_splits) {

@@ -487,6 +487,9 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
     if (threadIdx.x == 0) atomicCAS(p.status, 0, kDevBadCluster);
     return;
   }
+  // A merge kernel queued behind this grid may be placed on SMs as CTAs of this
+  // grid finish (it waits for the whole grid before reading anything).
+  ptx::griddep_launch_dependents();
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -1265,6 +1268,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
   extern __shared__ float sm[];
   float* wts = sm;                          // [n_splits] weights, then the total l
   float4* acc_w = reinterpret_cast<float4*>(sm + ((n_splits + 4) & ~3));  // [8][32]
+  // Launched as a programmatic dependent of the attention grid: wait until that
+  // grid has completed and its partials are visible.
+  ptx::griddep_wait();
   const long long row = blockIdx.x;
   const int c0 = blockIdx.y * 128;
   const int t = threadIdx.x, warp = t / 32, lane = t % 32;
