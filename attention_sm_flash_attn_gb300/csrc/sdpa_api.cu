@@ -28,8 +28,8 @@ struct DeviceState {
   bool ready = false;
   int sms = 0;
   int* status = nullptr;  // device address of g_device_status
-  bool attr_set[6] = {false, false, false, false, false, false};
-  int sk_units[6] = {0, 0, 0, 0, 0, 0};  // resident persistent units per variant
+  bool attr_set[24] = {};   // per kernel instantiation (variant_index)
+  int sk_units[24] = {};    // resident persistent units per instantiation
   unsigned long long epoch = 0;          // last persistent-launch epoch handed out
 };
 
@@ -87,6 +87,8 @@ int encode_map(CUtensorMap* m, const void* base, int D, long long L, long long B
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+bool supported_head_dim(int D) { return D == 128 || D == 192 || D == 256 || D == 512; }
+
 int validate(const void* q, const void* k, const void* v, const void* out, int B, int Hq, int Hkv,
              int Lq, int Lk, int D, float scale, int causal, int window, int dtype) {
   if (!q || !k || !v || !out) return SDPA_ERR_INVALID_ARG;
@@ -96,7 +98,7 @@ int validate(const void* q, const void* k, const void* v, const void* out, int B
   if (window < 0 || (window > 0 && !causal)) return SDPA_ERR_INVALID_ARG;
   if (causal && Lq > Lk) return SDPA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || scale < 0.f) return SDPA_ERR_INVALID_ARG;
-  if (D != 256 && D != 512) return SDPA_ERR_UNSUPPORTED;
+  if (!supported_head_dim(D)) return SDPA_ERR_UNSUPPORTED;
   if (dtype != SDPA_F16 && dtype != SDPA_BF16) return SDPA_ERR_UNSUPPORTED;
   // TMA coordinates and flat row indices stay within 32-bit / 64-bit ranges.
   if (static_cast<long long>(B) * Hq > (1ll << 30) || static_cast<long long>(B) * Hkv > (1ll << 30))
@@ -106,26 +108,34 @@ int validate(const void* q, const void* k, const void* v, const void* out, int B
   return SDPA_OK;
 }
 
-template <bool BF16, int MODE>
+// Slot of a kernel instantiation in the per-device tables: dtype x variant x
+// per-CTA head dim (256, 128, 192).
+template <bool BF16, int MODE, int HD>
+constexpr int variant_index() {
+  return (BF16 ? 1 : 0) + 2 * (MODE * 3 + (HD == 256 ? 0 : HD == 128 ? 1 : 2));
+}
+constexpr int kNumVariants = 2 * 4 * 3;  // the tables in DeviceState
+
+template <bool BF16, int MODE, int HD>
 int ensure_attr(DeviceState* st) {
-  const int idx = (BF16 ? 1 : 0) + 2 * MODE;
+  const int idx = variant_index<BF16, MODE, HD>();
   if (st->attr_set[idx]) return SDPA_OK;
-  auto kern = gbsdpa::attn_fwd_kernel<BF16, MODE>;
+  auto kern = gbsdpa::attn_fwd_kernel<BF16, MODE, HD>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg<BF16, MODE>::SMEM_BYTES) != cudaSuccess)
+                           Cfg<BF16, MODE, HD>::SMEM_BYTES) != cudaSuccess)
     return SDPA_ERR_CUDA;
   st->attr_set[idx] = true;
   return SDPA_OK;
 }
 
-template <bool BF16, int MODE>
+template <bool BF16, int MODE, int HD>
 void fill_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, long long ctas,
                  cudaStream_t stream) {
   constexpr bool kCluster = MODE != gbsdpa::kSingle;
   *cfg = {};
   cfg->gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
-  cfg->blockDim = dim3(Cfg<BF16, MODE>::NTHREADS, 1, 1);
-  cfg->dynamicSmemBytes = Cfg<BF16, MODE>::SMEM_BYTES;
+  cfg->blockDim = dim3(Cfg<BF16, MODE, HD>::NTHREADS, 1, 1);
+  cfg->dynamicSmemBytes = Cfg<BF16, MODE, HD>::SMEM_BYTES;
   cfg->stream = stream;
   cfg->attrs = attr;
   cfg->numAttrs = 0;
@@ -138,9 +148,9 @@ void fill_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, long long c
   }
 }
 
-template <bool BF16, int MODE>
+template <bool BF16, int MODE, int HD>
 int launch_attn(const AttnParams& p, long long items, cudaStream_t stream, DeviceState* st) {
-  int rc = ensure_attr<BF16, MODE>(st);
+  int rc = ensure_attr<BF16, MODE, HD>(st);
   if (rc) return rc;
   constexpr bool kCluster = MODE != gbsdpa::kSingle;
   const long long ctas = items * (kCluster ? 2 : 1);
@@ -151,32 +161,32 @@ int launch_attn(const AttnParams& p, long long items, cudaStream_t stream, Devic
   // sized to the occupancy limit, so on an otherwise idle GPU all of it is
   // resident; the kernel starts the never-waiting units first, and a wait that
   // still runs out reports a device timeout instead of hanging.
-  fill_launch<BF16, MODE>(&cfg, attr, ctas, stream);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gbsdpa::attn_fwd_kernel<BF16, MODE>, p);
+  fill_launch<BF16, MODE, HD>(&cfg, attr, ctas, stream);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gbsdpa::attn_fwd_kernel<BF16, MODE, HD>, p);
   return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
 // How many persistent units (CTAs, or CTA pairs for the 2-SM variant) can be
 // resident at once on this device; 0 if the variant cannot run persistently.
-template <bool BF16, int MODE>
+template <bool BF16, int MODE, int HD>
 int resident_units(DeviceState* st) {
-  const int idx = (BF16 ? 1 : 0) + 2 * MODE;
+  const int idx = variant_index<BF16, MODE, HD>();
   if (st->sk_units[idx]) return st->sk_units[idx];
-  if (ensure_attr<BF16, MODE>(st)) return 0;
+  if (ensure_attr<BF16, MODE, HD>(st)) return 0;
   int units = 0;
   if (MODE == gbsdpa::kSingle) {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gbsdpa::attn_fwd_kernel<BF16, MODE>,
-                                                      Cfg<BF16, MODE>::NTHREADS,
-                                                      Cfg<BF16, MODE>::SMEM_BYTES) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gbsdpa::attn_fwd_kernel<BF16, MODE, HD>,
+                                                      Cfg<BF16, MODE, HD>::NTHREADS,
+                                                      Cfg<BF16, MODE, HD>::SMEM_BYTES) != cudaSuccess)
       return 0;
     units = per_sm * st->sms;
   } else {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
-    fill_launch<BF16, MODE>(&cfg, attr, 2 * (st->sms / 2), nullptr);
+    fill_launch<BF16, MODE, HD>(&cfg, attr, 2 * (st->sms / 2), nullptr);
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, gbsdpa::attn_fwd_kernel<BF16, MODE>, &cfg) !=
+    if (cudaOccupancyMaxActiveClusters(&clusters, gbsdpa::attn_fwd_kernel<BF16, MODE, HD>, &cfg) !=
         cudaSuccess)
       return 0;
     units = clusters;
@@ -189,11 +199,11 @@ int launch_combine(const float* part_o, const float* part_ml, void* out, long lo
                    int n_splits, bool bf16, cudaStream_t stream) {
   // weights (n_splits + 1, padded to 4 floats) then 8 x 32 float4 warp sums
   const size_t sh = static_cast<size_t>((n_splits + 4) & ~3) * sizeof(float) + 8 * 32 * 16;
-  if (R <= 0 || R > 0x7fffffffll || D % 128 != 0) return SDPA_ERR_INVALID_ARG;
+  if (R <= 0 || R > 0x7fffffffll || D % 64 != 0) return SDPA_ERR_INVALID_ARG;
   // Programmatic dependent launch: the merge grid's CTAs may be placed while the
   // attention grid drains; the kernel waits for that grid before reading.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(R), static_cast<unsigned>(D / 128));
+  cfg.gridDim = dim3(static_cast<unsigned>(R), static_cast<unsigned>((D + 127) / 128));
   cfg.blockDim = dim3(gbsdpa::kCombineThreads, 1, 1);
   cfg.dynamicSmemBytes = sh;
   cfg.stream = stream;
@@ -217,15 +227,18 @@ size_t partial_bytes(long long R, int D, int n_splits) {
 }
 
 // Kernel variant for a call: head_dim 512 splits the head dimension over a CTA
-// pair; head_dim 256 prefill uses 2-SM MMAs over 256-row query tiles (a 2-SM
-// tile costs about two thirds of two 1-SM tiles), except with a sliding window
-// shorter than 256 keys, where most of a 256-row tile's keys would be masked;
+// pair; head_dim 256 and 128 prefill use 2-SM MMAs over 256-row query tiles (a
+// 2-SM tile costs about two thirds of two 1-SM tiles), except with a sliding
+// window shorter than 256 keys, where most of a 256-row tile's keys would be
+// masked; head_dim 192 prefill stays on one CTA (the 2-SM tile would split V
+// into 96-column halves, which a 128-byte-swizzled 64-column box cannot hold);
 // decode uses one CTA per 16 query heads x 8 position slots.
 int choose_mode(bool decode, int D, int window) {
   if (D == 512) return gbsdpa::kPair;
-  if (decode) return gbsdpa::kSingle;
+  if (decode || D == 192) return gbsdpa::kSingle;
   return (window > 0 && window < 256) ? gbsdpa::kSingle : gbsdpa::kDuo;
 }
+
 
 int qtile_rows(int mode) { return mode == gbsdpa::kDuo ? 256 : 128; }
 int key_tile(int mode) { return mode == gbsdpa::kPair ? 64 : 128; }
@@ -370,11 +383,17 @@ TailPlan plan_tail(long long units, int B, int Hq, int Lq, int Lk, int causal, i
 
 // Units for a persistent prefill launch (0: one CTA per query tile instead).
 template <bool BF16>
-long long persistent_units(DeviceState* st, int mode, int B, int Hq, int Lq, int Lk, int causal,
-                           int window) {
+long long persistent_units(DeviceState* st, int mode, int D, int B, int Hq, int Lq, int Lk,
+                           int causal, int window) {
   int units = 0;
-  if (mode == gbsdpa::kSingle) units = resident_units<BF16, gbsdpa::kSingle>(st);
-  else if (mode == gbsdpa::kDuo) units = resident_units<BF16, gbsdpa::kDuo>(st);
+  if (mode == gbsdpa::kSingle) {
+    units = D == 128   ? resident_units<BF16, gbsdpa::kSingle, 128>(st)
+            : D == 192 ? resident_units<BF16, gbsdpa::kSingle, 192>(st)
+                       : resident_units<BF16, gbsdpa::kSingle, 256>(st);
+  } else if (mode == gbsdpa::kDuo) {
+    units = D == 128 ? resident_units<BF16, gbsdpa::kDuo, 128>(st)
+                     : resident_units<BF16, gbsdpa::kDuo, 256>(st);
+  }
   else return 0;
   if (units <= 0) return 0;
   const long long W =
@@ -453,9 +472,16 @@ int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, i
   else
     items = static_cast<long long>(B) * Hq * p.n_qtiles * n_splits;
   switch (mode) {
-    case gbsdpa::kPair: rc = launch_attn<BF16, gbsdpa::kPair>(p, items, stream, st); break;
-    case gbsdpa::kDuo: rc = launch_attn<BF16, gbsdpa::kDuo>(p, items, stream, st); break;
-    default: rc = launch_attn<BF16, gbsdpa::kSingle>(p, items, stream, st); break;
+    case gbsdpa::kPair: rc = launch_attn<BF16, gbsdpa::kPair, 256>(p, items, stream, st); break;
+    case gbsdpa::kDuo:
+      rc = D == 128 ? launch_attn<BF16, gbsdpa::kDuo, 128>(p, items, stream, st)
+                    : launch_attn<BF16, gbsdpa::kDuo, 256>(p, items, stream, st);
+      break;
+    default:
+      rc = D == 128   ? launch_attn<BF16, gbsdpa::kSingle, 128>(p, items, stream, st)
+           : D == 192 ? launch_attn<BF16, gbsdpa::kSingle, 192>(p, items, stream, st)
+                      : launch_attn<BF16, gbsdpa::kSingle, 256>(p, items, stream, st);
+      break;
   }
   if (rc) return rc;
   if (write_partial)
@@ -471,13 +497,13 @@ size_t sdpa_prefill_workspace_bytes(int B, int Hq, int Hkv, int Lq, int Lk, int 
                                     int window) {
   DeviceState* st = nullptr;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lk <= 0 || Hq % Hkv) return 0;
-  if (D != 256 && D != 512) return 0;
+  if (!supported_head_dim(D)) return 0;
   if (causal != 0 && causal != 1) return 0;
   if (window < 0 || (causal && Lq > Lk)) return 0;
   if (device_state(&st)) return 0;
   const int mode = choose_mode(false, D, causal ? window : 0);
-  const long long u = std::max(persistent_units<false>(st, mode, B, Hq, Lq, Lk, causal, window),
-                               persistent_units<true>(st, mode, B, Hq, Lq, Lk, causal, window));
+  const long long u = std::max(persistent_units<false>(st, mode, D, B, Hq, Lq, Lk, causal, window),
+                               persistent_units<true>(st, mode, D, B, Hq, Lq, Lk, causal, window));
   if (u > 0) return sk_layout(u).bytes;
   const int s = plan_prefill_splits(st->sms, B, Hq, Lq, Lk, D, causal, window);
   if (s <= 1) return 0;
@@ -490,12 +516,12 @@ int sdpa_prefill_launches(int B, int Hq, int Hkv, int Lq, int Lk, int D, int cau
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lk <= 0 || Hq % Hkv) return SDPA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return SDPA_ERR_INVALID_ARG;
   if (window < 0 || (window > 0 && !causal) || (causal && Lq > Lk)) return SDPA_ERR_INVALID_ARG;
-  if (D != 256 && D != 512) return SDPA_ERR_UNSUPPORTED;
+  if (!supported_head_dim(D)) return SDPA_ERR_UNSUPPORTED;
   DeviceState* st = nullptr;
   int rc = device_state(&st);
   if (rc) return rc;
   const int mode = choose_mode(false, D, window);
-  const long long u = persistent_units<false>(st, mode, B, Hq, Lq, Lk, causal, window);
+  const long long u = persistent_units<false>(st, mode, D, B, Hq, Lq, Lk, causal, window);
   if (u > 0) return 1;  // persistent with the workspace, one CTA per tile without
   const int s = plan_prefill_splits(st->sms, B, Hq, Lq, Lk, D, causal, window);
   return (s > 1 && workspace_bytes >= partial_bytes(static_cast<long long>(B) * Hq * Lq, D, s))
@@ -505,7 +531,7 @@ int sdpa_prefill_launches(int B, int Hq, int Hkv, int Lq, int Lk, int D, int cau
 size_t sdpa_decode_workspace_bytes(int B, int Hq, int Hkv, int Lq, int D) {
   DeviceState* st = nullptr;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lq > 8 || Hq % Hkv) return 0;
-  if (D != 256 && D != 512) return 0;
+  if (!supported_head_dim(D)) return 0;
   if (device_state(&st)) return 0;
   const int s = plan_decode_splits(st->sms, B, Hq, Hkv, D);
   return partial_bytes(static_cast<long long>(B) * Hq * Lq, D, s);
@@ -523,8 +549,8 @@ int sdpa_prefill(const void* q, const void* k, const void* v, void* out, int B, 
   const bool bf16 = dtype == SDPA_BF16;
   auto strm = reinterpret_cast<cudaStream_t>(stream);
   const int mode = choose_mode(false, D, window);
-  const long long u = bf16 ? persistent_units<true>(st, mode, B, Hq, Lq, Lk, causal, window)
-                           : persistent_units<false>(st, mode, B, Hq, Lq, Lk, causal, window);
+  const long long u = bf16 ? persistent_units<true>(st, mode, D, B, Hq, Lq, Lk, causal, window)
+                           : persistent_units<false>(st, mode, D, B, Hq, Lq, Lk, causal, window);
   if (u > 0 && workspace && workspace_bytes >= sk_layout(u).bytes)
     return bf16 ? run<true>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, false, 1,
                             false, workspace, strm, st, 0, u)

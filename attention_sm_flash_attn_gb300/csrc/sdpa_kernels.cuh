@@ -111,12 +111,12 @@ struct AttnParams {
 //            tile, which halves the bytes each SM stages per FLOP.
 enum Mode : int { kSingle = 0, kPair = 1, kDuo = 2 };
 
-template <bool BF16, int MODE>
+template <bool BF16, int MODE, int HD = 256>
 struct Cfg {
   static constexpr bool PAIR = MODE == kPair;
   static constexpr bool DUO = MODE == kDuo;
   static constexpr int BM = 128;                   // query rows per CTA
-  static constexpr int DH = 256;                   // head-dim columns owned by one CTA
+  static constexpr int DH = HD;                    // head-dim columns owned by one CTA
   static constexpr int BN = PAIR ? 64 : 128;       // keys per tile
   static constexpr int HB = BN / 2;                // key columns per softmax thread
   static constexpr int NSLOT = PAIR ? 5 : 8;
@@ -128,9 +128,12 @@ struct Cfg {
   // V per CTA and tile: DUO holds 128 of the 256 head-dim columns for all keys,
   // in slots of 64 keys x 128 columns; the others hold slots of 32 keys x 256.
   static constexpr int VROWS = DUO ? 64 : 32;      // keys per V slot (= rows of a V box)
-  static constexpr int VBOX = DUO ? 2 : 4;         // 64-column V boxes per slot
+  static constexpr int VBOX = (DUO ? DH / 2 : DH) / 64;  // 64-column V boxes per slot
   static constexpr int VSUB = BN / VROWS;          // V slots per tile
   static constexpr int V_LBO = VROWS * 128;        // bytes between 64-column V boxes
+  // Bytes one CTA loads into a ring slot (a V slot is not full below head_dim 256).
+  static constexpr int K_SLOT_BYTES = KBOX * KROWS * 128;
+  static constexpr int V_SLOT_BYTES = VBOX * V_LBO;
   static constexpr int Q_OFF = 0;
   static constexpr int RING_OFF = 65536;
   static constexpr int P_OFF = RING_OFF + NSLOT * SLOT;
@@ -156,13 +159,18 @@ struct Cfg {
   static constexpr int kMmaWarp = 9;
   static constexpr int MMA_M = DUO ? 256 : 128;
   static constexpr uint32_t IDESC_QK = ptx::idesc_f16(MMA_M, BN, BF16, false, false);
-  static constexpr uint32_t IDESC_PV = ptx::idesc_f16(MMA_M, DUO ? 2 * 128 : DH, BF16, false, true);
+  // P.V: N = DH (the 2-SM variant's B operand is two DH/2-column halves).
+  static constexpr uint32_t IDESC_PV = ptx::idesc_f16(MMA_M, DH, BF16, false, true);
+  static constexpr int Q_BYTES = BM * DH * 2;  // one CTA's query tile
   // Arrivals completing P-full on the MMA CTA: one per softmax warp of each CTA
   // whose P rows the MMA reads.
   static constexpr int kPFullArrivals = DUO ? 16 : 8;
   static_assert(S_COL + 2 * BN <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(KSUB * KBOX * 64 == DH && VSUB * VROWS == BN, "tile decomposition");
+  static_assert(VBOX * 64 == (DUO ? DH / 2 : DH) && V_SLOT_BYTES <= SLOT && K_SLOT_BYTES == SLOT,
+                "K/V slot layout");
+  static_assert(Q_BYTES <= RING_OFF && (!PAIR || DH == 256), "query tile / pair head dim");
 };
 
 // Barrier slots inside the barrier area.
@@ -455,9 +463,9 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
   }
 }
 
-template <bool BF16, int MODE>
+template <bool BF16, int MODE, int HD>
 __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
-  using C = Cfg<BF16, MODE>;
+  using C = Cfg<BF16, MODE, HD>;
   constexpr bool PAIR = C::PAIR;
   constexpr bool DUO = C::DUO;
   constexpr bool CLUSTER = PAIR || DUO;
@@ -587,12 +595,12 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
             break;
           }
           const uint32_t qbar = leader_bar(kBarQ);
-          if (mma_cta) ptx::mbar_arrive_expect_tx(bar(kBarQ), DUO ? 2 * 65536 : 65536);
-          for (int c = 0; c < 4; ++c)
+          if (mma_cta) ptx::mbar_arrive_expect_tx(bar(kBarQ), DUO ? 2 * C::Q_BYTES : C::Q_BYTES);
+          for (int c = 0; c < C::DH / 64; ++c)
             load(sQ + c * 16384, &p.tm_q, qbar, d0 + c * 64, w.m0, bh_q);
           ++issued_q;
         }
-        auto next_slot = [&](int& slot, uint32_t& fullbar) -> bool {
+        auto next_slot = [&](int& slot, uint32_t& fullbar, uint32_t bytes) -> bool {
           slot = n % C::NSLOT;
           if (!wait_bar(bar(kBarKvEmpty + slot), ((n / C::NSLOT) & 1) ^ 1, abort_flag, p.status,
                         kDevTimeoutKvEmpty))
@@ -600,7 +608,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
           fullbar = leader_bar(kBarKvFull + slot);
           // The MMA CTA posts the bytes of both halves (DUO) on its own barrier.
           if (mma_cta)
-            ptx::mbar_arrive_expect_tx(bar(kBarKvFull + slot), DUO ? 2 * C::SLOT : C::SLOT);
+            ptx::mbar_arrive_expect_tx(bar(kBarKvFull + slot), DUO ? 2 * bytes : bytes);
           return true;
         };
         auto load_k = [&](int j) {
@@ -610,7 +618,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
           for (int ks = 0; ks < C::KSUB && ok; ++ks, ++n) {
             int slot;
             uint32_t fb;
-            if (!next_slot(slot, fb)) {
+            if (!next_slot(slot, fb, C::K_SLOT_BYTES)) {
               ok = false;
               break;
             }
@@ -621,13 +629,13 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
           }
         };
         auto load_v = [&](int j) {
-          // DUO: CTA `rank` loads head-dim columns [128 rank, 128 rank + 128) of V.
+          // DUO: CTA `rank` loads head-dim columns [DH/2 rank, DH/2 (rank + 1)) of V.
           const int key0 = (w.t_begin + j * w.t_step) * BN;
-          const int dv0 = DUO ? static_cast<int>(rank) * 128 : d0;
+          const int dv0 = DUO ? static_cast<int>(rank) * (C::DH / 2) : d0;
           for (int vs = 0; vs < C::VSUB && ok; ++vs, ++n) {
             int slot;
             uint32_t fb;
-            if (!next_slot(slot, fb)) {
+            if (!next_slot(slot, fb, C::V_SLOT_BYTES)) {
               ok = false;
               break;
             }
@@ -1255,7 +1263,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
 
 // Merge split partials: for each row, M = max_s m_s, l = sum_s 2^(m_s - M) l_s,
 // out = sum_s 2^(m_s - M) O_s / l, splits that saw no visible key (l_s == 0)
-// skipped.  Grid (rows, D / 128); 256 threads: warp w accumulates splits
+// skipped.  Grid (rows, ceil(D / 128)); 256 threads: warp w accumulates splits
 // w, w+8, w+16, ... for 128 columns (4 per lane), then the eight warp sums are
 // added in warp order.  The maximum is a warp-shuffle reduction; every sum runs
 // in a fixed order, so a row's result depends only on that row's partials.
@@ -1274,6 +1282,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
   const long long row = blockIdx.x;
   const int c0 = blockIdx.y * 128;
   const int t = threadIdx.x, warp = t / 32, lane = t % 32;
+  const bool col_ok = c0 + 4 * lane < D;  // head_dim 192: the second block is half full
   if (warp == 0) {
     float mx = -INFINITY;
     for (int s = lane; s < n_splits; s += 32) {
@@ -1298,7 +1307,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
   const float* base = part_o + row * D + c0 + 4 * lane;
   const long long split_stride = R * D;
-  for (int s0 = warp; s0 < n_splits; s0 += 8 * 4) {
+  // (head_dim 192: lanes past the last column sit the loop out)
+  for (int s0 = warp; col_ok && s0 < n_splits; s0 += 8 * 4) {
     float4 v[4];
     float wv[4];
 #pragma unroll
@@ -1333,7 +1343,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     uint2 o;
     o.x = pack2(sum.x * inv, sum.y * inv, BF16);
     o.y = pack2(sum.z * inv, sum.w * inv, BF16);
-    *reinterpret_cast<uint2*>(out + row * D + c0 + 4 * lane) = o;
+    if (col_ok) *reinterpret_cast<uint2*>(out + row * D + c0 + 4 * lane) = o;
   }
 }
 

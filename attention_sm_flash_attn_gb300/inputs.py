@@ -70,8 +70,17 @@ DECODE_SLIDING = Workload("decode_sliding_w1024_hd256_k128k", 1, 16, 8, 1, 13107
 DECODE_FULL512 = Workload("decode_full_hd512_k128k", 1, 16, 1, 1, 131072, 512,
                           torch.float16, True, 0, 53, kind="decode")
 
-PREFILL_WORKLOADS = [TINY, TINY_W32, LONGKV, SELF16K, SLIDING32K, FULL512, PREFILL128K]
-DECODE_WORKLOADS = [DECODE_SLIDING, DECODE_FULL512]
+# head_dim 192, which "Fused SDPA full-attention for head_dim=192/256" (MLX PR
+# #3660) serves alongside 256, and 128 as a regression shape: the long-KV GQA
+# geometry above at those head dims.
+LONGKV_HD192 = LONGKV.with_(name="longkv_gqa_prefill_hd192", D=192, seed=61)
+LONGKV_HD128 = LONGKV.with_(name="longkv_gqa_prefill_hd128", D=128, seed=62)
+DECODE_SLIDING_HD192 = DECODE_SLIDING.with_(name="decode_sliding_w1024_hd192_k128k", D=192,
+                                            seed=63)
+
+PREFILL_WORKLOADS = [TINY, TINY_W32, LONGKV, SELF16K, SLIDING32K, FULL512, PREFILL128K,
+                     LONGKV_HD192, LONGKV_HD128]
+DECODE_WORKLOADS = [DECODE_SLIDING, DECODE_FULL512, DECODE_SLIDING_HD192]
 DECODE_LQ = (1, 2, 4, 8)
 
 

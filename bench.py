@@ -238,7 +238,8 @@ def cpu_baseline(w, q, k, v, budget_s=12.0, max_rows=None):
 
 def suite(gb, device, flush, stream, hbm, bf16_peak):
     res = {}
-    for w in [wl.LONGKV, wl.SELF16K, wl.SLIDING32K, wl.FULL512, wl.PREFILL128K]:
+    for w in [wl.LONGKV, wl.SELF16K, wl.SLIDING32K, wl.FULL512, wl.PREFILL128K,
+              wl.LONGKV_HD192, wl.LONGKV_HD128]:
         q, k, v = wl.make_qkv(w, device=device)
         out = torch.empty_like(q)
         ws = torch.empty(max(1, gb.prefill_workspace_bytes(w.B, w.Hq, w.Hkv, w.Lq, w.Lk, w.D,

@@ -42,7 +42,10 @@
  *  allocates device memory: where split partials are needed the caller passes
  *  a workspace of at least the size the matching *_workspace_bytes call
  *  returns (that size does not grow with Lk).
- *  Supported: D in {256, 512}; dtype SDPA_F16 or SDPA_BF16.
+ *  Supported: D in {128, 192, 256, 512}; dtype SDPA_F16 or SDPA_BF16.  256
+ *  and 512 are the pages' head dims; 192 is the head dim "Fused SDPA
+ *  full-attention for head_dim=192/256" (MLX PR #3660) also serves, and 128
+ *  is kept as a regression shape.
  *
  * Errors
  * ------

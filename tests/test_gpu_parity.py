@@ -3,9 +3,9 @@
 Tolerance (max abs error on unit-variance inputs): 4e-3 for fp16, 1.6e-2 for
 bf16.  Cases span several 128-row query tiles and 128-key tiles with ragged
 tails, grouped-query heads, bottom-right causal masks, sliding windows, the
-split-KV prefill path, both head dims and both dtypes.  Exact pins: one key
-(Lk = 1) and window 1 make every softmax weight exactly 1, so the GPU output
-must equal the value row bit for bit.
+split and persistent prefill paths, every head dim (128, 192, 256, 512) and
+both dtypes.  Exact pins: one key (Lk = 1) and window 1 make every softmax
+weight exactly 1, so the GPU output must equal the value row bit for bit.
 """
 import math
 
@@ -48,6 +48,18 @@ PREFILL_CASES = [
     (1, 2, 2, 70, 129, 512, False, 0),
     (1, 2, 1, 129, 4100, 256, True, 0),     # long keys: split-KV prefill + combine
     (1, 2, 1, 256, 3000, 512, True, 0),     # long keys at head_dim 512
+    # head_dim 192 (one-CTA variant) and 128 (2-SM variant, one CTA for short windows)
+    (1, 2, 1, 128, 128, 192, True, 0),
+    (1, 4, 2, 200, 333, 192, True, 0),
+    (1, 2, 2, 300, 300, 192, True, 7),
+    (2, 2, 1, 130, 257, 192, False, 0),
+    (1, 2, 1, 129, 4100, 192, True, 0),
+    (1, 2, 1, 128, 128, 128, True, 0),
+    (1, 4, 2, 200, 333, 128, True, 0),
+    (2, 2, 1, 130, 257, 128, False, 0),
+    (1, 4, 1, 64, 700, 128, True, 100),
+    (1, 2, 2, 600, 1500, 128, True, 300),
+    (1, 2, 1, 129, 4100, 128, True, 0),
 ]
 
 
@@ -90,7 +102,7 @@ def test_prefill_without_workspace_matches_split_path(case):
     assert max_err(out, ref) < 4e-3
 
 
-@pytest.mark.parametrize("D", [256, 512])
+@pytest.mark.parametrize("D", [128, 192, 256, 512])
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
 def test_single_key_is_exact(D, dtype):
     q, k, v = draw(1, 4, 2, 5, 1, D, dtype, seed=11)
@@ -99,7 +111,7 @@ def test_single_key_is_exact(D, dtype):
     assert torch.equal(out.cpu(), want)
 
 
-@pytest.mark.parametrize("D", [256, 512])
+@pytest.mark.parametrize("D", [128, 192, 256, 512])
 def test_window_one_is_exact(D):
     Lq, Lk = 150, 300
     q, k, v = draw(1, 2, 1, Lq, Lk, D, torch.bfloat16, seed=12)
@@ -125,6 +137,8 @@ DECODE_CASES = [
     (2, 4, 2, 777, 256, 0),
     (1, 32, 1, 1000, 256, 0),    # 32 query heads per kv head: two head blocks
     (1, 4, 4, 129, 512, 64),
+    (1, 16, 8, 5000, 192, 1024),
+    (2, 8, 2, 777, 128, 0),
 ]
 
 

@@ -1,4 +1,4 @@
-"""GPU parity of the persistent prefill schedule (head_dim 256 with a workspace).
+"""GPU parity of the persistent prefill schedule (head_dim 128/192/256 with a workspace).
 
 Resident units take the query tiles in waves, then share the leftover partial
 wave by key tiles: a leftover tile's prefix stays on one unit, its suffix is cut
@@ -54,11 +54,8 @@ def rows_to_check(B, Hq, Lq, seed):
     return np.unique(np.asarray(ids, dtype=np.int64))
 
 
-@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
-@pytest.mark.parametrize("case", CASES)
-def test_persistent_prefill_matches_oracle(case, dtype):
+def check_against_oracle(case, dtype, D):
     B, Hq, Hkv, Lq, Lk, causal, window = case
-    D = 256
     assert gb.prefill_workspace_bytes(B, Hq, Hkv, Lq, Lk, D, causal, window) > 0
     q, k, v = draw(B, Hq, Hkv, Lq, Lk, D, dtype, seed=sum(case))
     scale = 1.0 / math.sqrt(D)
@@ -71,6 +68,19 @@ def test_persistent_prefill_matches_oracle(case, dtype):
     got = out.reshape(-1, D)[torch.as_tensor(ids, device=DEV)].double().cpu().numpy()
     err = float(np.max(np.abs(got - ref)))
     assert err < TOL[dtype], f"max abs err {err}"
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("case", CASES)
+def test_persistent_prefill_matches_oracle(case, dtype):
+    check_against_oracle(case, dtype, 256)
+
+
+@pytest.mark.parametrize("D", [128, 192])
+@pytest.mark.parametrize("case", [CASES[0], CASES[3]])
+def test_persistent_prefill_other_head_dims(case, D):
+    """head_dim 128 runs the 2-SM variant, 192 the one-CTA variant."""
+    check_against_oracle(case, torch.float16, D)
 
 
 def test_persistent_prefill_is_deterministic_and_ignores_stale_flags():

@@ -20,8 +20,7 @@ pytestmark = pytest.mark.gpu
 TOL = {torch.float16: 4e-3, torch.bfloat16: 1.6e-2}
 
 
-@pytest.mark.parametrize("w", [wl.TINY, wl.TINY_W32, wl.LONGKV, wl.SELF16K, wl.SLIDING32K,
-                               wl.FULL512, wl.PREFILL128K], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", wl.PREFILL_WORKLOADS, ids=lambda w: w.name)
 def test_prefill_workload_sampled_rows(w):
     q, k, v = wl.make_qkv(w, device="cuda")
     out = gb.sdpa_prefill(q, k, v, scale=w.scale, causal=w.causal, window=w.window)

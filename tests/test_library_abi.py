@@ -59,7 +59,8 @@ BAD = [
     (dict(q=None), -1), (dict(B=0), -1), (dict(Hq=3, Hkv=2), -1), (dict(Lk=0), -1),
     (dict(causal=2), -1), (dict(window=-1), -1), (dict(causal=0, window=4), -1),
     (dict(Lq=9, Lk=8), -1), (dict(scale=-1.0), -1), (dict(scale=float("nan")), -1),
-    (dict(D=128), -2), (dict(D=192), -2), (dict(dtype=2), -2), (dict(k=ODD), -6),
+    (dict(D=64), -2), (dict(D=96), -2), (dict(D=320), -2), (dict(dtype=2), -2),
+    (dict(k=ODD), -6),
 ]
 
 
@@ -80,11 +81,11 @@ def test_decode_requires_a_workspace(lib):
 def test_workspace_queries_reject_bad_shapes(lib):
     assert lib.sdpa_decode_workspace_bytes(1, 3, 2, 1, 256) == 0
     assert lib.sdpa_decode_workspace_bytes(1, 2, 1, 9, 256) == 0
-    assert lib.sdpa_prefill_workspace_bytes(1, 2, 1, 4, 8, 128, 1, 0) == 0
+    assert lib.sdpa_prefill_workspace_bytes(1, 2, 1, 4, 8, 96, 1, 0) == 0
 
 
 def test_launch_query_rejects_bad_arguments_on_the_host(lib):
-    assert lib.sdpa_prefill_launches(1, 2, 1, 4, 8, 128, 1, 0, 0) == -2   # head dim
+    assert lib.sdpa_prefill_launches(1, 2, 1, 4, 8, 96, 1, 0, 0) == -2    # head dim
     assert lib.sdpa_prefill_launches(1, 3, 2, 4, 8, 256, 1, 0, 0) == -1   # Hq % Hkv
     assert lib.sdpa_prefill_launches(1, 2, 1, 4, 8, 256, 0, 16, 0) == -1  # window w/o causal
     assert lib.sdpa_prefill_launches(1, 2, 1, 9, 8, 256, 1, 0, 0) == -1   # causal Lq > Lk
