@@ -25,7 +25,7 @@ __all__ = [
 
 SDPA_F16, SDPA_BF16 = 0, 1
 EXPORTED_SYMBOLS = ("sdpa_prefill", "sdpa_prefill_workspace_bytes", "sdpa_prefill_launches",
-                    "sdpa_decode",
+                    "sdpa_prefill_kv", "sdpa_decode_kv", "sdpa_decode",
                     "sdpa_decode_workspace_bytes", "sdpa_device_status", "sdpa_status_string",
                     "sdpa_version", "sdpa_decode_noalloc", "sdpa_selftest_timeout")
 # Size of the library-resident scratch used by sdpa_decode_noalloc (see the header).
@@ -61,6 +61,11 @@ def load_library(path: str | None = None):
         lib.sdpa_prefill.restype = i
         lib.sdpa_decode.argtypes = attn
         lib.sdpa_decode.restype = i
+        attn_kv = attn[:14] + [i, i] + attn[14:]
+        lib.sdpa_prefill_kv.argtypes = attn_kv
+        lib.sdpa_prefill_kv.restype = i
+        lib.sdpa_decode_kv.argtypes = attn_kv
+        lib.sdpa_decode_kv.restype = i
         lib.sdpa_prefill_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
         lib.sdpa_prefill_workspace_bytes.restype = sz
         lib.sdpa_prefill_launches.argtypes = [i, i, i, i, i, i, i, i, sz]
@@ -104,7 +109,7 @@ def _stream_ptr(stream) -> int:
     return int(stream.cuda_stream)
 
 
-def _check(q, k, v, out):
+def _check(q, k, v, out, lk=None):
     for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
         if not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor")
@@ -115,9 +120,10 @@ def _check(q, k, v, out):
     if not (q.dtype == k.dtype == v.dtype == out.dtype):
         raise TypeError("q, k, v, out must share one dtype")
     B, Hq, Lq, D = q.shape
-    _, Hkv, Lk, _ = k.shape
-    if tuple(k.shape) != (B, Hkv, Lk, D) or tuple(v.shape) != (B, Hkv, Lk, D):
-        raise ValueError("k and v must be [B, Hkv, Lk, D] with q's B and D")
+    _, Hkv, L, _ = k.shape  # Lk keys, or the capacity of a K/V cache
+    if tuple(k.shape) != (B, Hkv, L, D) or tuple(v.shape) != (B, Hkv, L, D):
+        raise ValueError("k and v must be [B, Hkv, L, D] with q's B and D")
+    Lk = L if lk is None else int(lk)
     if tuple(out.shape) != tuple(q.shape):
         raise ValueError("out must have q's shape")
     return B, Hq, Hkv, Lq, Lk, D
@@ -149,49 +155,57 @@ def _workspace(nbytes: int, device, workspace):
     return workspace
 
 
+def _call(entry, kv_entry, q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, lk,
+          ring, workspace, stream):
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    lib = load_library()
+    common = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, Hq, Hkv, Lq, Lk, D,
+              float(scale), int(bool(causal)), int(window), _dtype_code(q))
+    if lk is None and not ring:
+        rc = getattr(lib, entry)(*common, ws_ptr, ws_len, _stream_ptr(stream))
+        name = entry
+    else:
+        rc = getattr(lib, kv_entry)(*common, int(k.shape[2]), int(bool(ring)), ws_ptr, ws_len,
+                                    _stream_ptr(stream))
+        name = kv_entry
+    if rc != 0:
+        raise SdpaError(rc, name)
+    return out
+
+
 def sdpa_prefill(q, k, v, out=None, *, scale=None, causal=False, window=0, workspace=None,
-                 stream=None):
+                 stream=None, lk=None, ring=False):
     """Fused attention over [B, H, L, D] fp16/bf16 CUDA tensors (see sdpa_prefill in
     include/sdpa_gb300.h).  Returns ``out``.  ``workspace`` may be a uint8 CUDA
-    tensor; when None one is allocated with torch if the split plan wants it."""
+    tensor; when None one is allocated with torch if the schedule wants it.
+    With ``lk`` given (or ``ring``), k and v are a K/V cache of k.shape[2] rows
+    holding Lk = lk keys (see sdpa_prefill_kv)."""
     if out is None:
         out = torch.empty_like(q)
-    B, Hq, Hkv, Lq, Lk, D = _check(q, k, v, out)
+    B, Hq, Hkv, Lq, Lk, D = _check(q, k, v, out, lk)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     need = prefill_workspace_bytes(B, Hq, Hkv, Lq, Lk, D, causal, window)
     workspace = _workspace(need, q.device, workspace)
-    ws_ptr = workspace.data_ptr() if workspace is not None else None
-    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    rc = load_library().sdpa_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                                      B, Hq, Hkv, Lq, Lk, D, float(scale), int(bool(causal)),
-                                      int(window), _dtype_code(q), ws_ptr, ws_len,
-                                      _stream_ptr(stream))
-    if rc != 0:
-        raise SdpaError(rc, "sdpa_prefill")
-    return out
+    return _call("sdpa_prefill", "sdpa_prefill_kv", q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale,
+                 causal, window, lk, ring, workspace, stream)
 
 
 def sdpa_decode(q, k, v, out=None, *, scale=None, causal=True, window=0, workspace=None,
-                stream=None):
+                stream=None, lk=None, ring=False):
     """Split-KV decode / verify for 1 <= Lq <= 8 (see sdpa_decode in
-    include/sdpa_gb300.h).  Returns ``out``."""
+    include/sdpa_gb300.h).  Returns ``out``.  ``lk`` / ``ring`` as for
+    sdpa_prefill (see sdpa_decode_kv)."""
     if out is None:
         out = torch.empty_like(q)
-    B, Hq, Hkv, Lq, Lk, D = _check(q, k, v, out)
+    B, Hq, Hkv, Lq, Lk, D = _check(q, k, v, out, lk)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     need = decode_workspace_bytes(B, Hq, Hkv, Lq, D)
     workspace = _workspace(need, q.device, workspace)
-    ws_ptr = workspace.data_ptr() if workspace is not None else None
-    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    rc = load_library().sdpa_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                                     B, Hq, Hkv, Lq, Lk, D, float(scale), int(bool(causal)),
-                                     int(window), _dtype_code(q), ws_ptr, ws_len,
-                                     _stream_ptr(stream))
-    if rc != 0:
-        raise SdpaError(rc, "sdpa_decode")
-    return out
+    return _call("sdpa_decode", "sdpa_decode_kv", q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale,
+                 causal, window, lk, ring, workspace, stream)
 
 
 def device_status(stream=None):

@@ -71,11 +71,14 @@ int device_state(DeviceState** out) {
 // 3-D map over a contiguous [BH, L, D] tensor: dims (D, L, BH), box (64, rows, 1),
 // 128-byte swizzle; rows past L read as zero and never spill into the next head.
 int encode_map(CUtensorMap* m, const void* base, int D, long long L, long long BH, int rows,
-               bool bf16) {
+               bool bf16, long long plane_rows = 0) {
+  // plane_rows: rows from one (b, h) plane to the next (L for a packed tensor;
+  // a K/V cache's capacity otherwise).
+  if (plane_rows <= 0) plane_rows = L;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
-                           static_cast<cuuint64_t>(L) * static_cast<cuuint64_t>(D) * 2};
+                           static_cast<cuuint64_t>(plane_rows) * static_cast<cuuint64_t>(D) * 2};
   cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows), 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
@@ -110,6 +113,21 @@ int validate(const void* q, const void* k, const void* v, const void* out, int B
 
 // Slot of a kernel instantiation in the per-device tables: dtype x variant x
 // per-CTA head dim (256, 128, 192).
+// K/V in a cache of kv_cap rows per (b, kv head): packed rows 0..Lk-1
+// (kv_cap >= Lk), or a ring where key j sits in row j mod kv_cap.  A ring must
+// hold every key some row can see (the window plus the query rows, or all Lk
+// keys without a window) and a multiple of 128 rows, so that no key tile wraps.
+int validate_kv_layout(int Lq, int Lk, int causal, int window, int kv_cap, int kv_ring) {
+  if (kv_ring != 0 && kv_ring != 1) return SDPA_ERR_INVALID_ARG;
+  if (kv_cap <= 0 || kv_cap > (1 << 30)) return SDPA_ERR_INVALID_ARG;
+  if (!kv_ring) return kv_cap >= Lk ? SDPA_OK : SDPA_ERR_INVALID_ARG;
+  if (kv_cap % 128 != 0) return SDPA_ERR_INVALID_ARG;
+  const long long span = (causal && window > 0)
+                             ? std::min<long long>(Lk, static_cast<long long>(Lq) + window - 1)
+                             : Lk;
+  return span <= kv_cap ? SDPA_OK : SDPA_ERR_INVALID_ARG;
+}
+
 template <bool BF16, int MODE, int HD>
 constexpr int variant_index() {
   return (BF16 ? 1 : 0) + 2 * (MODE * 3 + (HD == 256 ? 0 : HD == 128 ? 1 : 2));
@@ -405,7 +423,7 @@ template <bool BF16>
 int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv, int Lq,
         int Lk, int D, float scale, int causal, int window, bool decode, int n_splits,
         bool write_partial, void* workspace, cudaStream_t stream, DeviceState* st,
-        int withhold_q = 0, long long sk_units = 0) {
+        int withhold_q = 0, long long sk_units = 0, int kv_cap = 0, int kv_ring = 0) {
   AttnParams p;
   std::memset(&p, 0, sizeof(p));
   const int mode = choose_mode(decode, D, window);
@@ -416,10 +434,15 @@ int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, i
   int rc = SDPA_OK;
   if (!decode) rc = encode_map(&p.tm_q, q, D, Lq, static_cast<long long>(B) * Hq, 128, BF16);
   if (rc) return rc;
-  rc = encode_map(&p.tm_k, k, D, Lk, static_cast<long long>(B) * Hkv, k_rows, BF16);
+  // K/V: Lk keys packed, or in a cache of kv_cap rows per plane (a ring keeps
+  // all kv_cap rows live).
+  if (kv_cap <= 0) kv_cap = Lk;
+  const long long kv_rows = kv_ring ? kv_cap : Lk;
+  rc = encode_map(&p.tm_k, k, D, kv_rows, static_cast<long long>(B) * Hkv, k_rows, BF16, kv_cap);
   if (rc) return rc;
-  rc = encode_map(&p.tm_v, v, D, Lk, static_cast<long long>(B) * Hkv, v_rows, BF16);
+  rc = encode_map(&p.tm_v, v, D, kv_rows, static_cast<long long>(B) * Hkv, v_rows, BF16, kv_cap);
   if (rc) return rc;
+  p.kv_ring = kv_ring ? kv_cap : 0;
   const long long R = static_cast<long long>(B) * Hq * Lq;
   p.q = static_cast<const uint16_t*>(q);
   p.out = static_cast<uint16_t*>(out);
@@ -537,10 +560,13 @@ size_t sdpa_decode_workspace_bytes(int B, int Hq, int Hkv, int Lq, int D) {
   return partial_bytes(static_cast<long long>(B) * Hq * Lq, D, s);
 }
 
-int sdpa_prefill(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
-                 int Lq, int Lk, int D, float scale, int causal, int window, int dtype,
-                 void* workspace, size_t workspace_bytes, sdpa_stream_t stream) {
+static int prefill_impl(const void* q, const void* k, const void* v, void* out, int B, int Hq,
+                        int Hkv, int Lq, int Lk, int D, float scale, int causal, int window,
+                        int dtype, int kv_cap, int kv_ring, void* workspace,
+                        size_t workspace_bytes, sdpa_stream_t stream) {
   int rc = validate(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, dtype);
+  if (rc) return rc;
+  rc = validate_kv_layout(Lq, Lk, causal, window, kv_cap, kv_ring);
   if (rc) return rc;
   if (workspace && !aligned16(workspace)) return SDPA_ERR_ALIGNMENT;
   DeviceState* st = nullptr;
@@ -553,23 +579,26 @@ int sdpa_prefill(const void* q, const void* k, const void* v, void* out, int B, 
                            : persistent_units<false>(st, mode, D, B, Hq, Lq, Lk, causal, window);
   if (u > 0 && workspace && workspace_bytes >= sk_layout(u).bytes)
     return bf16 ? run<true>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, false, 1,
-                            false, workspace, strm, st, 0, u)
+                            false, workspace, strm, st, 0, u, kv_cap, kv_ring)
                 : run<false>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, false, 1,
-                             false, workspace, strm, st, 0, u);
+                             false, workspace, strm, st, 0, u, kv_cap, kv_ring);
   int s = u > 0 ? 1 : plan_prefill_splits(st->sms, B, Hq, Lq, Lk, D, causal, window);
   if (s > 1 && (!workspace ||
                 workspace_bytes < partial_bytes(static_cast<long long>(B) * Hq * Lq, D, s)))
     s = 1;
   return bf16 ? run<true>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, false, s,
-                          s > 1, workspace, strm, st)
+                          s > 1, workspace, strm, st, 0, 0, kv_cap, kv_ring)
               : run<false>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, false, s,
-                           s > 1, workspace, strm, st);
+                           s > 1, workspace, strm, st, 0, 0, kv_cap, kv_ring);
 }
 
-int sdpa_decode(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
-                int Lq, int Lk, int D, float scale, int causal, int window, int dtype,
-                void* workspace, size_t workspace_bytes, sdpa_stream_t stream) {
+static int decode_impl(const void* q, const void* k, const void* v, void* out, int B, int Hq,
+                       int Hkv, int Lq, int Lk, int D, float scale, int causal, int window,
+                       int dtype, int kv_cap, int kv_ring, void* workspace,
+                       size_t workspace_bytes, sdpa_stream_t stream) {
   int rc = validate(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, dtype);
+  if (rc) return rc;
+  rc = validate_kv_layout(Lq, Lk, causal, window, kv_cap, kv_ring);
   if (rc) return rc;
   if (Lq > 8) return SDPA_ERR_INVALID_ARG;
   if (!workspace) return SDPA_ERR_WORKSPACE;
@@ -583,9 +612,39 @@ int sdpa_decode(const void* q, const void* k, const void* v, void* out, int B, i
   const bool bf16 = dtype == SDPA_BF16;
   auto strm = reinterpret_cast<cudaStream_t>(stream);
   return bf16 ? run<true>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, true, s,
-                          true, workspace, strm, st)
+                          true, workspace, strm, st, 0, 0, kv_cap, kv_ring)
               : run<false>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, true, s,
-                           true, workspace, strm, st);
+                           true, workspace, strm, st, 0, 0, kv_cap, kv_ring);
+}
+
+int sdpa_prefill(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
+                 int Lq, int Lk, int D, float scale, int causal, int window, int dtype,
+                 void* workspace, size_t workspace_bytes, sdpa_stream_t stream) {
+  return prefill_impl(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, dtype, Lk, 0,
+                      workspace, workspace_bytes, stream);
+}
+
+int sdpa_decode(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
+                int Lq, int Lk, int D, float scale, int causal, int window, int dtype,
+                void* workspace, size_t workspace_bytes, sdpa_stream_t stream) {
+  return decode_impl(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, dtype, Lk, 0,
+                     workspace, workspace_bytes, stream);
+}
+
+int sdpa_prefill_kv(const void* q, const void* k, const void* v, void* out, int B, int Hq,
+                    int Hkv, int Lq, int Lk, int D, float scale, int causal, int window,
+                    int dtype, int kv_capacity, int kv_ring, void* workspace,
+                    size_t workspace_bytes, sdpa_stream_t stream) {
+  return prefill_impl(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, dtype,
+                      kv_capacity, kv_ring, workspace, workspace_bytes, stream);
+}
+
+int sdpa_decode_kv(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
+                   int Lq, int Lk, int D, float scale, int causal, int window, int dtype,
+                   int kv_capacity, int kv_ring, void* workspace, size_t workspace_bytes,
+                   sdpa_stream_t stream) {
+  return decode_impl(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, dtype,
+                     kv_capacity, kv_ring, workspace, workspace_bytes, stream);
 }
 
 int sdpa_device_status(sdpa_stream_t stream, int* detail) {

@@ -84,6 +84,9 @@ struct AttnParams {
   // "query tile ready" signal, so the MMA issuer's bounded wait runs out and the
   // kernel reports a device timeout instead of computing.
   int withhold_q;
+  // K/V rows: key j is row j of its (b, kv head) plane, or, for a ring buffer of
+  // kv_ring rows (a multiple of 128), row j mod kv_ring.
+  int kv_ring;
   // Persistent prefill (SINGLE and DUO variants): `n_units` resident CTAs (CTA
   // pairs for DUO) walk the query tiles ("items") in waves, then share out the
   // leftover partial wave so that every unit gets about the same number of key
@@ -600,6 +603,9 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
             load(sQ + c * 16384, &p.tm_q, qbar, d0 + c * 64, w.m0, bh_q);
           ++issued_q;
         }
+        // Row of the first key of a tile (tiles never straddle a ring's end: the
+        // ring length is a multiple of 128 and tiles start at multiples of BN).
+        auto kv_row = [&](int key) -> int { return p.kv_ring ? key % p.kv_ring : key; };
         auto next_slot = [&](int& slot, uint32_t& fullbar, uint32_t bytes) -> bool {
           slot = n % C::NSLOT;
           if (!wait_bar(bar(kBarKvEmpty + slot), ((n / C::NSLOT) & 1) ^ 1, abort_flag, p.status,
@@ -614,7 +620,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
         auto load_k = [&](int j) {
           // DUO: CTA `rank` loads keys [64 rank, 64 rank + 64) of the 128-key tile.
           const int key0 =
-              (w.t_begin + j * w.t_step) * BN + (DUO ? static_cast<int>(rank) * 64 : 0);
+              kv_row((w.t_begin + j * w.t_step) * BN) + (DUO ? static_cast<int>(rank) * 64 : 0);
           for (int ks = 0; ks < C::KSUB && ok; ++ks, ++n) {
             int slot;
             uint32_t fb;
@@ -630,7 +636,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
         };
         auto load_v = [&](int j) {
           // DUO: CTA `rank` loads head-dim columns [DH/2 rank, DH/2 (rank + 1)) of V.
-          const int key0 = (w.t_begin + j * w.t_step) * BN;
+          const int key0 = kv_row((w.t_begin + j * w.t_step) * BN);
           const int dv0 = DUO ? static_cast<int>(rank) * (C::DH / 2) : d0;
           for (int vs = 0; vs < C::VSUB && ok; ++vs, ++n) {
             int slot;

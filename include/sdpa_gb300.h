@@ -141,6 +141,39 @@ int sdpa_decode(const void* q, const void* k, const void* v, void* out, int B, i
 /* Workspace bytes sdpa_decode needs on the current device (0 on bad arguments). */
 size_t sdpa_decode_workspace_bytes(int B, int Hq, int Hkv, int Lq, int D);
 
+/*
+ * K/V read from a caller's cache instead of packed [B, Hkv, Lk, D] tensors.
+ *
+ * The pages' serving code decodes against KV caches: classic decode and the
+ * per-row verify calls read "strided, sliced keys", and sliding-window layers
+ * keep their keys in a ring addressed by a cursor ("fix: Gemma 4 MTP never
+ * engages on CUDA (GB10), verify probe fails", sections "Current Behavior"
+ * and "Proposed Solution"; a wrapped ring and an unwrapped one are both edge
+ * cases in "Implementation Notes").
+ *
+ * k, v  [B, Hkv, kv_capacity, D] contiguous, same dtype as q; only the rows
+ *       below are read.
+ * kv_ring = 0: key j (0 <= j < Lk) is row j; kv_capacity >= Lk.
+ * kv_ring = 1: key j is row (j mod kv_capacity): the cache holds the last
+ *       kv_capacity keys.  kv_capacity must be a multiple of 128 and hold every
+ *       key some query row can see: min(Lk, Lq + window - 1) keys with a window,
+ *       all Lk keys without one.  Rows of the ring that no query row can see
+ *       are read but weighted by exactly 0; they must hold finite values.
+ * Everything else is as for sdpa_prefill / sdpa_decode (same workspace sizes);
+ * the results equal, bit for bit, the calls on packed copies of the same keys,
+ * so decode row invariance holds over the trimmed prefix of the same cache.
+ * Layout errors return SDPA_ERR_INVALID_ARG before anything is queued.
+ */
+int sdpa_prefill_kv(const void* q, const void* k, const void* v, void* out, int B, int Hq,
+                    int Hkv, int Lq, int Lk, int D, float scale, int causal, int window,
+                    int dtype, int kv_capacity, int kv_ring, void* workspace,
+                    size_t workspace_bytes, sdpa_stream_t stream);
+
+int sdpa_decode_kv(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
+                   int Lq, int Lk, int D, float scale, int causal, int window, int dtype,
+                   int kv_capacity, int kv_ring, void* workspace, size_t workspace_bytes,
+                   sdpa_stream_t stream);
+
 /* Synchronises `stream`, returns SDPA_OK or SDPA_ERR_DEVICE_TIMEOUT for the
  * current device and clears the status word.  *detail (if not NULL) receives
  * the raw device code (0 if none): 0x100..0x10a identify the pipeline wait that
