@@ -25,7 +25,7 @@ __all__ = [
 
 SDPA_F16, SDPA_BF16 = 0, 1
 EXPORTED_SYMBOLS = ("sdpa_prefill", "sdpa_prefill_workspace_bytes", "sdpa_prefill_launches",
-                    "sdpa_prefill_kv", "sdpa_decode_kv", "sdpa_decode",
+                    "sdpa_prefill_ex", "sdpa_decode_ex", "sdpa_decode",
                     "sdpa_decode_workspace_bytes", "sdpa_device_status", "sdpa_status_string",
                     "sdpa_version", "sdpa_decode_noalloc", "sdpa_selftest_timeout")
 # Size of the library-resident scratch used by sdpa_decode_noalloc (see the header).
@@ -61,11 +61,12 @@ def load_library(path: str | None = None):
         lib.sdpa_prefill.restype = i
         lib.sdpa_decode.argtypes = attn
         lib.sdpa_decode.restype = i
-        attn_kv = attn[:14] + [i, i] + attn[14:]
-        lib.sdpa_prefill_kv.argtypes = attn_kv
-        lib.sdpa_prefill_kv.restype = i
-        lib.sdpa_decode_kv.argtypes = attn_kv
-        lib.sdpa_decode_kv.restype = i
+        # ..., Lk, Dqk, Dv, scale, causal, window, dtype, kv_capacity, kv_ring, ws, bytes, stream
+        attn_ex = attn[:10] + [i] + attn[10:14] + [i, i] + attn[14:]
+        lib.sdpa_prefill_ex.argtypes = attn_ex
+        lib.sdpa_prefill_ex.restype = i
+        lib.sdpa_decode_ex.argtypes = attn_ex
+        lib.sdpa_decode_ex.restype = i
         lib.sdpa_prefill_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
         lib.sdpa_prefill_workspace_bytes.restype = sz
         lib.sdpa_prefill_launches.argtypes = [i, i, i, i, i, i, i, i, sz]
@@ -110,6 +111,8 @@ def _stream_ptr(stream) -> int:
 
 
 def _check(q, k, v, out, lk=None):
+    """Shapes: q [B, Hq, Lq, Dqk], k [B, Hkv, L, Dqk], v [B, Hkv, L, Dv], out [B, Hq,
+    Lq, Dv]; L is Lk, or the capacity of a K/V cache when ``lk`` is given."""
     for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
         if not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor")
@@ -120,13 +123,14 @@ def _check(q, k, v, out, lk=None):
     if not (q.dtype == k.dtype == v.dtype == out.dtype):
         raise TypeError("q, k, v, out must share one dtype")
     B, Hq, Lq, D = q.shape
-    _, Hkv, L, _ = k.shape  # Lk keys, or the capacity of a K/V cache
-    if tuple(k.shape) != (B, Hkv, L, D) or tuple(v.shape) != (B, Hkv, L, D):
-        raise ValueError("k and v must be [B, Hkv, L, D] with q's B and D")
+    _, Hkv, L, _ = k.shape
+    Dv = v.shape[3]
+    if tuple(k.shape) != (B, Hkv, L, D) or tuple(v.shape) != (B, Hkv, L, Dv):
+        raise ValueError("k must be [B, Hkv, L, Dqk] and v [B, Hkv, L, Dv] with q's B and Dqk")
+    if tuple(out.shape) != (B, Hq, Lq, Dv):
+        raise ValueError("out must be [B, Hq, Lq, Dv]")
     Lk = L if lk is None else int(lk)
-    if tuple(out.shape) != tuple(q.shape):
-        raise ValueError("out must have q's shape")
-    return B, Hq, Hkv, Lq, Lk, D
+    return B, Hq, Hkv, Lq, Lk, D, Dv
 
 
 def prefill_workspace_bytes(B, Hq, Hkv, Lq, Lk, D, causal=False, window=0) -> int:
@@ -155,57 +159,62 @@ def _workspace(nbytes: int, device, workspace):
     return workspace
 
 
-def _call(entry, kv_entry, q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, lk,
+def _call(entry, ex_entry, q, k, v, out, B, Hq, Hkv, Lq, Lk, D, Dv, scale, causal, window, lk,
           ring, workspace, stream):
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
     lib = load_library()
-    common = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, Hq, Hkv, Lq, Lk, D,
-              float(scale), int(bool(causal)), int(window), _dtype_code(q))
-    if lk is None and not ring:
-        rc = getattr(lib, entry)(*common, ws_ptr, ws_len, _stream_ptr(stream))
+    head = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, Hq, Hkv, Lq, Lk, D)
+    tail = (float(scale), int(bool(causal)), int(window), _dtype_code(q))
+    if lk is None and not ring and Dv == D:
+        rc = getattr(lib, entry)(*head, *tail, ws_ptr, ws_len, _stream_ptr(stream))
         name = entry
     else:
-        rc = getattr(lib, kv_entry)(*common, int(k.shape[2]), int(bool(ring)), ws_ptr, ws_len,
-                                    _stream_ptr(stream))
-        name = kv_entry
+        rc = getattr(lib, ex_entry)(*head, Dv, *tail, int(k.shape[2]), int(bool(ring)), ws_ptr,
+                                    ws_len, _stream_ptr(stream))
+        name = ex_entry
     if rc != 0:
         raise SdpaError(rc, name)
     return out
 
 
+def _out(q, v, out):
+    if out is None:
+        out = torch.empty(q.shape[:3] + (v.shape[3],), dtype=q.dtype, device=q.device)
+    return out
+
+
 def sdpa_prefill(q, k, v, out=None, *, scale=None, causal=False, window=0, workspace=None,
                  stream=None, lk=None, ring=False):
-    """Fused attention over [B, H, L, D] fp16/bf16 CUDA tensors (see sdpa_prefill in
-    include/sdpa_gb300.h).  Returns ``out``.  ``workspace`` may be a uint8 CUDA
-    tensor; when None one is allocated with torch if the schedule wants it.
-    With ``lk`` given (or ``ring``), k and v are a K/V cache of k.shape[2] rows
-    holding Lk = lk keys (see sdpa_prefill_kv)."""
-    if out is None:
-        out = torch.empty_like(q)
-    B, Hq, Hkv, Lq, Lk, D = _check(q, k, v, out, lk)
+    """Fused attention over [B, H, L, D] fp16/bf16 CUDA tensors (see sdpa_prefill and
+    sdpa_prefill_ex in include/sdpa_gb300.h).  Returns ``out``.  ``workspace`` may
+    be a uint8 CUDA tensor; when None one is allocated with torch if the schedule
+    wants it.  v may have its own head dim (Q/K 192 with V 256).  With ``lk``
+    given (or ``ring``), k and v are a K/V cache of k.shape[2] rows holding
+    Lk = lk keys."""
+    out = _out(q, v, out)
+    B, Hq, Hkv, Lq, Lk, D, Dv = _check(q, k, v, out, lk)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     need = prefill_workspace_bytes(B, Hq, Hkv, Lq, Lk, D, causal, window)
     workspace = _workspace(need, q.device, workspace)
-    return _call("sdpa_prefill", "sdpa_prefill_kv", q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale,
-                 causal, window, lk, ring, workspace, stream)
+    return _call("sdpa_prefill", "sdpa_prefill_ex", q, k, v, out, B, Hq, Hkv, Lq, Lk, D, Dv,
+                 scale, causal, window, lk, ring, workspace, stream)
 
 
 def sdpa_decode(q, k, v, out=None, *, scale=None, causal=True, window=0, workspace=None,
                 stream=None, lk=None, ring=False):
-    """Split-KV decode / verify for 1 <= Lq <= 8 (see sdpa_decode in
-    include/sdpa_gb300.h).  Returns ``out``.  ``lk`` / ``ring`` as for
-    sdpa_prefill (see sdpa_decode_kv)."""
-    if out is None:
-        out = torch.empty_like(q)
-    B, Hq, Hkv, Lq, Lk, D = _check(q, k, v, out, lk)
+    """Split-KV decode / verify for 1 <= Lq <= 8 (see sdpa_decode and sdpa_decode_ex
+    in include/sdpa_gb300.h).  Returns ``out``.  Head dims, ``lk`` and ``ring`` as
+    for sdpa_prefill."""
+    out = _out(q, v, out)
+    B, Hq, Hkv, Lq, Lk, D, Dv = _check(q, k, v, out, lk)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    need = decode_workspace_bytes(B, Hq, Hkv, Lq, D)
+    need = decode_workspace_bytes(B, Hq, Hkv, Lq, Dv)
     workspace = _workspace(need, q.device, workspace)
-    return _call("sdpa_decode", "sdpa_decode_kv", q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale,
-                 causal, window, lk, ring, workspace, stream)
+    return _call("sdpa_decode", "sdpa_decode_ex", q, k, v, out, B, Hq, Hkv, Lq, Lk, D, Dv,
+                 scale, causal, window, lk, ring, workspace, stream)
 
 
 def device_status(stream=None):

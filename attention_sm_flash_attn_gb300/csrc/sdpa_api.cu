@@ -28,8 +28,8 @@ struct DeviceState {
   bool ready = false;
   int sms = 0;
   int* status = nullptr;  // device address of g_device_status
-  bool attr_set[24] = {};   // per kernel instantiation (variant_index)
-  int sk_units[24] = {};    // resident persistent units per instantiation
+  bool attr_set[32] = {};   // per kernel instantiation (variant_index)
+  int sk_units[32] = {};    // resident persistent units per instantiation
   unsigned long long epoch = 0;          // last persistent-launch epoch handed out
 };
 
@@ -117,6 +117,12 @@ int validate(const void* q, const void* k, const void* v, const void* out, int B
 // (kv_cap >= Lk), or a ring where key j sits in row j mod kv_cap.  A ring must
 // hold every key some row can see (the window plus the query rows, or all Lk
 // keys without a window) and a multiple of 128 rows, so that no key tile wraps.
+// Head dims: Q/K and V equal (128, 192, 256, 512), or Q/K 192 with V 256.
+int validate_dims(int Dqk, int Dv) {
+  if (Dqk == Dv) return SDPA_OK;  // checked with the rest of the arguments
+  return (Dqk == 192 && Dv == 256) ? SDPA_OK : SDPA_ERR_UNSUPPORTED;
+}
+
 int validate_kv_layout(int Lq, int Lk, int causal, int window, int kv_cap, int kv_ring) {
   if (kv_ring != 0 && kv_ring != 1) return SDPA_ERR_INVALID_ARG;
   if (kv_cap <= 0 || kv_cap > (1 << 30)) return SDPA_ERR_INVALID_ARG;
@@ -128,32 +134,41 @@ int validate_kv_layout(int Lq, int Lk, int causal, int window, int kv_cap, int k
   return span <= kv_cap ? SDPA_OK : SDPA_ERR_INVALID_ARG;
 }
 
-template <bool BF16, int MODE, int HD>
+// Slot of a kernel instantiation in the per-device tables: dtype x variant x
+// per-CTA head dims (Q/K, V): (256, 256), (128, 128), (192, 192), (192, 256).
+template <bool BF16, int MODE, int HD, int HDV>
 constexpr int variant_index() {
-  return (BF16 ? 1 : 0) + 2 * (MODE * 3 + (HD == 256 ? 0 : HD == 128 ? 1 : 2));
+  return (BF16 ? 1 : 0) +
+         2 * (MODE * 4 + (HD != HDV ? 3 : HD == 256 ? 0 : HD == 128 ? 1 : 2));
 }
-constexpr int kNumVariants = 2 * 4 * 3;  // the tables in DeviceState
+constexpr int kNumVariants = 2 * 4 * 4;
+static_assert(sizeof(DeviceState::attr_set) == kNumVariants * sizeof(bool) &&
+                  sizeof(DeviceState::sk_units) == kNumVariants * sizeof(int),
+              "one table entry per kernel instantiation");
+static_assert(variant_index<false, gbsdpa::kSingle, 192, 256>() !=
+                  variant_index<false, gbsdpa::kSingle, 192, 192>(),
+              "distinct slots");
 
-template <bool BF16, int MODE, int HD>
+template <bool BF16, int MODE, int HD, int HDV>
 int ensure_attr(DeviceState* st) {
-  const int idx = variant_index<BF16, MODE, HD>();
+  const int idx = variant_index<BF16, MODE, HD, HDV>();
   if (st->attr_set[idx]) return SDPA_OK;
-  auto kern = gbsdpa::attn_fwd_kernel<BF16, MODE, HD>;
+  auto kern = gbsdpa::attn_fwd_kernel<BF16, MODE, HD, HDV>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg<BF16, MODE, HD>::SMEM_BYTES) != cudaSuccess)
+                           Cfg<BF16, MODE, HD, HDV>::SMEM_BYTES) != cudaSuccess)
     return SDPA_ERR_CUDA;
   st->attr_set[idx] = true;
   return SDPA_OK;
 }
 
-template <bool BF16, int MODE, int HD>
+template <bool BF16, int MODE, int HD, int HDV>
 void fill_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, long long ctas,
                  cudaStream_t stream) {
   constexpr bool kCluster = MODE != gbsdpa::kSingle;
   *cfg = {};
   cfg->gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
-  cfg->blockDim = dim3(Cfg<BF16, MODE, HD>::NTHREADS, 1, 1);
-  cfg->dynamicSmemBytes = Cfg<BF16, MODE, HD>::SMEM_BYTES;
+  cfg->blockDim = dim3(Cfg<BF16, MODE, HD, HDV>::NTHREADS, 1, 1);
+  cfg->dynamicSmemBytes = Cfg<BF16, MODE, HD, HDV>::SMEM_BYTES;
   cfg->stream = stream;
   cfg->attrs = attr;
   cfg->numAttrs = 0;
@@ -166,9 +181,9 @@ void fill_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, long long c
   }
 }
 
-template <bool BF16, int MODE, int HD>
+template <bool BF16, int MODE, int HD, int HDV>
 int launch_attn(const AttnParams& p, long long items, cudaStream_t stream, DeviceState* st) {
-  int rc = ensure_attr<BF16, MODE, HD>(st);
+  int rc = ensure_attr<BF16, MODE, HD, HDV>(st);
   if (rc) return rc;
   constexpr bool kCluster = MODE != gbsdpa::kSingle;
   const long long ctas = items * (kCluster ? 2 : 1);
@@ -179,32 +194,32 @@ int launch_attn(const AttnParams& p, long long items, cudaStream_t stream, Devic
   // sized to the occupancy limit, so on an otherwise idle GPU all of it is
   // resident; the kernel starts the never-waiting units first, and a wait that
   // still runs out reports a device timeout instead of hanging.
-  fill_launch<BF16, MODE, HD>(&cfg, attr, ctas, stream);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gbsdpa::attn_fwd_kernel<BF16, MODE, HD>, p);
+  fill_launch<BF16, MODE, HD, HDV>(&cfg, attr, ctas, stream);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gbsdpa::attn_fwd_kernel<BF16, MODE, HD, HDV>, p);
   return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
 // How many persistent units (CTAs, or CTA pairs for the 2-SM variant) can be
 // resident at once on this device; 0 if the variant cannot run persistently.
-template <bool BF16, int MODE, int HD>
+template <bool BF16, int MODE, int HD, int HDV>
 int resident_units(DeviceState* st) {
-  const int idx = variant_index<BF16, MODE, HD>();
+  const int idx = variant_index<BF16, MODE, HD, HDV>();
   if (st->sk_units[idx]) return st->sk_units[idx];
-  if (ensure_attr<BF16, MODE, HD>(st)) return 0;
+  if (ensure_attr<BF16, MODE, HD, HDV>(st)) return 0;
   int units = 0;
   if (MODE == gbsdpa::kSingle) {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gbsdpa::attn_fwd_kernel<BF16, MODE, HD>,
-                                                      Cfg<BF16, MODE, HD>::NTHREADS,
-                                                      Cfg<BF16, MODE, HD>::SMEM_BYTES) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gbsdpa::attn_fwd_kernel<BF16, MODE, HD, HDV>,
+                                                      Cfg<BF16, MODE, HD, HDV>::NTHREADS,
+                                                      Cfg<BF16, MODE, HD, HDV>::SMEM_BYTES) != cudaSuccess)
       return 0;
     units = per_sm * st->sms;
   } else {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
-    fill_launch<BF16, MODE, HD>(&cfg, attr, 2 * (st->sms / 2), nullptr);
+    fill_launch<BF16, MODE, HD, HDV>(&cfg, attr, 2 * (st->sms / 2), nullptr);
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, gbsdpa::attn_fwd_kernel<BF16, MODE, HD>, &cfg) !=
+    if (cudaOccupancyMaxActiveClusters(&clusters, gbsdpa::attn_fwd_kernel<BF16, MODE, HD, HDV>, &cfg) !=
         cudaSuccess)
       return 0;
     units = clusters;
@@ -402,15 +417,17 @@ TailPlan plan_tail(long long units, int B, int Hq, int Lq, int Lk, int causal, i
 // Units for a persistent prefill launch (0: one CTA per query tile instead).
 template <bool BF16>
 long long persistent_units(DeviceState* st, int mode, int D, int B, int Hq, int Lq, int Lk,
-                           int causal, int window) {
+                           int causal, int window, int Dv = 0) {
+  if (Dv <= 0) Dv = D;
   int units = 0;
   if (mode == gbsdpa::kSingle) {
-    units = D == 128   ? resident_units<BF16, gbsdpa::kSingle, 128>(st)
-            : D == 192 ? resident_units<BF16, gbsdpa::kSingle, 192>(st)
-                       : resident_units<BF16, gbsdpa::kSingle, 256>(st);
+    units = D != Dv    ? resident_units<BF16, gbsdpa::kSingle, 192, 256>(st)
+            : D == 128 ? resident_units<BF16, gbsdpa::kSingle, 128, 128>(st)
+            : D == 192 ? resident_units<BF16, gbsdpa::kSingle, 192, 192>(st)
+                       : resident_units<BF16, gbsdpa::kSingle, 256, 256>(st);
   } else if (mode == gbsdpa::kDuo) {
-    units = D == 128 ? resident_units<BF16, gbsdpa::kDuo, 128>(st)
-                     : resident_units<BF16, gbsdpa::kDuo, 256>(st);
+    units = D == 128 ? resident_units<BF16, gbsdpa::kDuo, 128, 128>(st)
+                     : resident_units<BF16, gbsdpa::kDuo, 256, 256>(st);
   }
   else return 0;
   if (units <= 0) return 0;
@@ -423,7 +440,9 @@ template <bool BF16>
 int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv, int Lq,
         int Lk, int D, float scale, int causal, int window, bool decode, int n_splits,
         bool write_partial, void* workspace, cudaStream_t stream, DeviceState* st,
-        int withhold_q = 0, long long sk_units = 0, int kv_cap = 0, int kv_ring = 0) {
+        int withhold_q = 0, long long sk_units = 0, int kv_cap = 0, int kv_ring = 0, int Dv = 0) {
+  // D is the Q/K head dim; Dv (0: the same) is V's and the output's.
+  if (Dv <= 0) Dv = D;
   AttnParams p;
   std::memset(&p, 0, sizeof(p));
   const int mode = choose_mode(decode, D, window);
@@ -440,14 +459,14 @@ int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, i
   const long long kv_rows = kv_ring ? kv_cap : Lk;
   rc = encode_map(&p.tm_k, k, D, kv_rows, static_cast<long long>(B) * Hkv, k_rows, BF16, kv_cap);
   if (rc) return rc;
-  rc = encode_map(&p.tm_v, v, D, kv_rows, static_cast<long long>(B) * Hkv, v_rows, BF16, kv_cap);
+  rc = encode_map(&p.tm_v, v, Dv, kv_rows, static_cast<long long>(B) * Hkv, v_rows, BF16, kv_cap);
   if (rc) return rc;
   p.kv_ring = kv_ring ? kv_cap : 0;
   const long long R = static_cast<long long>(B) * Hq * Lq;
   p.q = static_cast<const uint16_t*>(q);
   p.out = static_cast<uint16_t*>(out);
   if (write_partial) {
-    const size_t po = static_cast<size_t>(n_splits) * static_cast<size_t>(R) * D * sizeof(float);
+    const size_t po = static_cast<size_t>(n_splits) * static_cast<size_t>(R) * Dv * sizeof(float);
     p.part_o = static_cast<float*>(workspace);
     p.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                          ((po + 255) & ~static_cast<size_t>(255)));
@@ -459,7 +478,8 @@ int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, i
   p.G = Hq / Hkv;
   p.Lq = Lq;
   p.Lk = Lk;
-  p.D = D;
+  p.D = Dv;
+  p.Dqk = D;
   p.causal = causal;
   p.window = window;
   // c = scale * log2(e), kept > 0 so that a masked score (-inf) maps to -inf;
@@ -495,20 +515,21 @@ int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, i
   else
     items = static_cast<long long>(B) * Hq * p.n_qtiles * n_splits;
   switch (mode) {
-    case gbsdpa::kPair: rc = launch_attn<BF16, gbsdpa::kPair, 256>(p, items, stream, st); break;
+    case gbsdpa::kPair: rc = launch_attn<BF16, gbsdpa::kPair, 256, 256>(p, items, stream, st); break;
     case gbsdpa::kDuo:
-      rc = D == 128 ? launch_attn<BF16, gbsdpa::kDuo, 128>(p, items, stream, st)
-                    : launch_attn<BF16, gbsdpa::kDuo, 256>(p, items, stream, st);
+      rc = D == 128 ? launch_attn<BF16, gbsdpa::kDuo, 128, 128>(p, items, stream, st)
+                    : launch_attn<BF16, gbsdpa::kDuo, 256, 256>(p, items, stream, st);
       break;
     default:
-      rc = D == 128   ? launch_attn<BF16, gbsdpa::kSingle, 128>(p, items, stream, st)
-           : D == 192 ? launch_attn<BF16, gbsdpa::kSingle, 192>(p, items, stream, st)
-                      : launch_attn<BF16, gbsdpa::kSingle, 256>(p, items, stream, st);
+      rc = D != Dv    ? launch_attn<BF16, gbsdpa::kSingle, 192, 256>(p, items, stream, st)
+           : D == 128 ? launch_attn<BF16, gbsdpa::kSingle, 128, 128>(p, items, stream, st)
+           : D == 192 ? launch_attn<BF16, gbsdpa::kSingle, 192, 192>(p, items, stream, st)
+                      : launch_attn<BF16, gbsdpa::kSingle, 256, 256>(p, items, stream, st);
       break;
   }
   if (rc) return rc;
   if (write_partial)
-    rc = launch_combine(p.part_o, p.part_ml, out, R, D, n_splits, BF16, stream);
+    rc = launch_combine(p.part_o, p.part_ml, out, R, Dv, n_splits, BF16, stream);
   return rc;
 }
 
@@ -561,10 +582,12 @@ size_t sdpa_decode_workspace_bytes(int B, int Hq, int Hkv, int Lq, int D) {
 }
 
 static int prefill_impl(const void* q, const void* k, const void* v, void* out, int B, int Hq,
-                        int Hkv, int Lq, int Lk, int D, float scale, int causal, int window,
-                        int dtype, int kv_cap, int kv_ring, void* workspace,
+                        int Hkv, int Lq, int Lk, int D, int Dv, float scale, int causal,
+                        int window, int dtype, int kv_cap, int kv_ring, void* workspace,
                         size_t workspace_bytes, sdpa_stream_t stream) {
   int rc = validate(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, dtype);
+  if (rc) return rc;
+  rc = validate_dims(D, Dv);
   if (rc) return rc;
   rc = validate_kv_layout(Lq, Lk, causal, window, kv_cap, kv_ring);
   if (rc) return rc;
@@ -575,28 +598,30 @@ static int prefill_impl(const void* q, const void* k, const void* v, void* out, 
   const bool bf16 = dtype == SDPA_BF16;
   auto strm = reinterpret_cast<cudaStream_t>(stream);
   const int mode = choose_mode(false, D, window);
-  const long long u = bf16 ? persistent_units<true>(st, mode, D, B, Hq, Lq, Lk, causal, window)
-                           : persistent_units<false>(st, mode, D, B, Hq, Lq, Lk, causal, window);
+  const long long u = bf16 ? persistent_units<true>(st, mode, D, B, Hq, Lq, Lk, causal, window, Dv)
+                           : persistent_units<false>(st, mode, D, B, Hq, Lq, Lk, causal, window, Dv);
   if (u > 0 && workspace && workspace_bytes >= sk_layout(u).bytes)
     return bf16 ? run<true>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, false, 1,
-                            false, workspace, strm, st, 0, u, kv_cap, kv_ring)
+                            false, workspace, strm, st, 0, u, kv_cap, kv_ring, Dv)
                 : run<false>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, false, 1,
-                             false, workspace, strm, st, 0, u, kv_cap, kv_ring);
+                             false, workspace, strm, st, 0, u, kv_cap, kv_ring, Dv);
   int s = u > 0 ? 1 : plan_prefill_splits(st->sms, B, Hq, Lq, Lk, D, causal, window);
   if (s > 1 && (!workspace ||
-                workspace_bytes < partial_bytes(static_cast<long long>(B) * Hq * Lq, D, s)))
+                workspace_bytes < partial_bytes(static_cast<long long>(B) * Hq * Lq, Dv, s)))
     s = 1;
   return bf16 ? run<true>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, false, s,
-                          s > 1, workspace, strm, st, 0, 0, kv_cap, kv_ring)
+                          s > 1, workspace, strm, st, 0, 0, kv_cap, kv_ring, Dv)
               : run<false>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, false, s,
-                           s > 1, workspace, strm, st, 0, 0, kv_cap, kv_ring);
+                           s > 1, workspace, strm, st, 0, 0, kv_cap, kv_ring, Dv);
 }
 
 static int decode_impl(const void* q, const void* k, const void* v, void* out, int B, int Hq,
-                       int Hkv, int Lq, int Lk, int D, float scale, int causal, int window,
-                       int dtype, int kv_cap, int kv_ring, void* workspace,
+                       int Hkv, int Lq, int Lk, int D, int Dv, float scale, int causal,
+                       int window, int dtype, int kv_cap, int kv_ring, void* workspace,
                        size_t workspace_bytes, sdpa_stream_t stream) {
   int rc = validate(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, dtype);
+  if (rc) return rc;
+  rc = validate_dims(D, Dv);
   if (rc) return rc;
   rc = validate_kv_layout(Lq, Lk, causal, window, kv_cap, kv_ring);
   if (rc) return rc;
@@ -607,43 +632,43 @@ static int decode_impl(const void* q, const void* k, const void* v, void* out, i
   rc = device_state(&st);
   if (rc) return rc;
   const int s = plan_decode_splits(st->sms, B, Hq, Hkv, D);
-  if (workspace_bytes < partial_bytes(static_cast<long long>(B) * Hq * Lq, D, s))
+  if (workspace_bytes < partial_bytes(static_cast<long long>(B) * Hq * Lq, Dv, s))
     return SDPA_ERR_WORKSPACE;
   const bool bf16 = dtype == SDPA_BF16;
   auto strm = reinterpret_cast<cudaStream_t>(stream);
   return bf16 ? run<true>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, true, s,
-                          true, workspace, strm, st, 0, 0, kv_cap, kv_ring)
+                          true, workspace, strm, st, 0, 0, kv_cap, kv_ring, Dv)
               : run<false>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, true, s,
-                           true, workspace, strm, st, 0, 0, kv_cap, kv_ring);
+                           true, workspace, strm, st, 0, 0, kv_cap, kv_ring, Dv);
 }
 
 int sdpa_prefill(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
                  int Lq, int Lk, int D, float scale, int causal, int window, int dtype,
                  void* workspace, size_t workspace_bytes, sdpa_stream_t stream) {
-  return prefill_impl(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, dtype, Lk, 0,
+  return prefill_impl(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, D, scale, causal, window, dtype, Lk, 0,
                       workspace, workspace_bytes, stream);
 }
 
 int sdpa_decode(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
                 int Lq, int Lk, int D, float scale, int causal, int window, int dtype,
                 void* workspace, size_t workspace_bytes, sdpa_stream_t stream) {
-  return decode_impl(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, dtype, Lk, 0,
+  return decode_impl(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, D, scale, causal, window, dtype, Lk, 0,
                      workspace, workspace_bytes, stream);
 }
 
-int sdpa_prefill_kv(const void* q, const void* k, const void* v, void* out, int B, int Hq,
-                    int Hkv, int Lq, int Lk, int D, float scale, int causal, int window,
+int sdpa_prefill_ex(const void* q, const void* k, const void* v, void* out, int B, int Hq,
+                    int Hkv, int Lq, int Lk, int Dqk, int Dv, float scale, int causal, int window,
                     int dtype, int kv_capacity, int kv_ring, void* workspace,
                     size_t workspace_bytes, sdpa_stream_t stream) {
-  return prefill_impl(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, dtype,
+  return prefill_impl(q, k, v, out, B, Hq, Hkv, Lq, Lk, Dqk, Dv, scale, causal, window, dtype,
                       kv_capacity, kv_ring, workspace, workspace_bytes, stream);
 }
 
-int sdpa_decode_kv(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
-                   int Lq, int Lk, int D, float scale, int causal, int window, int dtype,
-                   int kv_capacity, int kv_ring, void* workspace, size_t workspace_bytes,
-                   sdpa_stream_t stream) {
-  return decode_impl(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, dtype,
+int sdpa_decode_ex(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
+                   int Lq, int Lk, int Dqk, int Dv, float scale, int causal, int window,
+                   int dtype, int kv_capacity, int kv_ring, void* workspace,
+                   size_t workspace_bytes, sdpa_stream_t stream) {
+  return decode_impl(q, k, v, out, B, Hq, Hkv, Lq, Lk, Dqk, Dv, scale, causal, window, dtype,
                      kv_capacity, kv_ring, workspace, workspace_bytes, stream);
 }
 

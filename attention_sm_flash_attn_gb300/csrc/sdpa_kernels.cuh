@@ -72,7 +72,8 @@ struct AttnParams {
   float* part_o;   // [n_splits][B*Hq*Lq][D]
   float* part_ml;  // [n_splits][B*Hq*Lq][2]  (running max in log2 units, sum)
   int* status;
-  int B, Hq, Hkv, G, Lq, Lk, D;
+  int B, Hq, Hkv, G, Lq, Lk, D;  // D: head dim of V and the output
+  int Dqk;                       // head dim of Q and K
   int causal, window;
   float c;        // scale * log2(e)
   int decode;     // 0 = prefill, 1 = decode
@@ -114,12 +115,13 @@ struct AttnParams {
 //            tile, which halves the bytes each SM stages per FLOP.
 enum Mode : int { kSingle = 0, kPair = 1, kDuo = 2 };
 
-template <bool BF16, int MODE, int HD = 256>
+template <bool BF16, int MODE, int HD = 256, int HDV = HD>
 struct Cfg {
   static constexpr bool PAIR = MODE == kPair;
   static constexpr bool DUO = MODE == kDuo;
   static constexpr int BM = 128;                   // query rows per CTA
-  static constexpr int DH = HD;                    // head-dim columns owned by one CTA
+  static constexpr int DH = HD;                    // Q/K head-dim columns owned by one CTA
+  static constexpr int DV = HDV;                   // V (and output) head-dim columns
   static constexpr int BN = PAIR ? 64 : 128;       // keys per tile
   static constexpr int HB = BN / 2;                // key columns per softmax thread
   static constexpr int NSLOT = PAIR ? 5 : 8;
@@ -131,7 +133,7 @@ struct Cfg {
   // V per CTA and tile: DUO holds 128 of the 256 head-dim columns for all keys,
   // in slots of 64 keys x 128 columns; the others hold slots of 32 keys x 256.
   static constexpr int VROWS = DUO ? 64 : 32;      // keys per V slot (= rows of a V box)
-  static constexpr int VBOX = (DUO ? DH / 2 : DH) / 64;  // 64-column V boxes per slot
+  static constexpr int VBOX = (DUO ? DV / 2 : DV) / 64;  // 64-column V boxes per slot
   static constexpr int VSUB = BN / VROWS;          // V slots per tile
   static constexpr int V_LBO = VROWS * 128;        // bytes between 64-column V boxes
   // Bytes one CTA loads into a ring slot (a V slot is not full below head_dim 256).
@@ -162,8 +164,8 @@ struct Cfg {
   static constexpr int kMmaWarp = 9;
   static constexpr int MMA_M = DUO ? 256 : 128;
   static constexpr uint32_t IDESC_QK = ptx::idesc_f16(MMA_M, BN, BF16, false, false);
-  // P.V: N = DH (the 2-SM variant's B operand is two DH/2-column halves).
-  static constexpr uint32_t IDESC_PV = ptx::idesc_f16(MMA_M, DH, BF16, false, true);
+  // P.V: N = DV (the 2-SM variant's B operand is two DV/2-column halves).
+  static constexpr uint32_t IDESC_PV = ptx::idesc_f16(MMA_M, DV, BF16, false, true);
   static constexpr int Q_BYTES = BM * DH * 2;  // one CTA's query tile
   // Arrivals completing P-full on the MMA CTA: one per softmax warp of each CTA
   // whose P rows the MMA reads.
@@ -171,9 +173,10 @@ struct Cfg {
   static_assert(S_COL + 2 * BN <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(KSUB * KBOX * 64 == DH && VSUB * VROWS == BN, "tile decomposition");
-  static_assert(VBOX * 64 == (DUO ? DH / 2 : DH) && V_SLOT_BYTES <= SLOT && K_SLOT_BYTES == SLOT,
+  static_assert(VBOX * 64 == (DUO ? DV / 2 : DV) && V_SLOT_BYTES <= SLOT && K_SLOT_BYTES == SLOT,
                 "K/V slot layout");
-  static_assert(Q_BYTES <= RING_OFF && (!PAIR || DH == 256), "query tile / pair head dim");
+  static_assert(Q_BYTES <= RING_OFF && (!PAIR || (DH == 256 && DV == 256)) && DV <= S_COL,
+                "query tile / pair head dim / O columns");
 };
 
 // Barrier slots inside the barrier area.
@@ -466,9 +469,9 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
   }
 }
 
-template <bool BF16, int MODE, int HD>
+template <bool BF16, int MODE, int HD, int HDV>
 __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
-  using C = Cfg<BF16, MODE, HD>;
+  using C = Cfg<BF16, MODE, HD, HDV>;
   constexpr bool PAIR = C::PAIR;
   constexpr bool DUO = C::DUO;
   constexpr bool CLUSTER = PAIR || DUO;
@@ -637,7 +640,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
         auto load_v = [&](int j) {
           // DUO: CTA `rank` loads head-dim columns [DH/2 rank, DH/2 (rank + 1)) of V.
           const int key0 = kv_row((w.t_begin + j * w.t_step) * BN);
-          const int dv0 = DUO ? static_cast<int>(rank) * (C::DH / 2) : d0;
+          const int dv0 = DUO ? static_cast<int>(rank) * (C::DV / 2) : d0;
           for (int vs = 0; vs < C::VSUB && ok; ++vs, ++n) {
             int slot;
             uint32_t fb;
@@ -854,7 +857,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
         if (count > 0) {
           // Decode: stage this thread's half of the row's query slice into the
           // swizzled Q tile (16-byte chunks of 8 elements).
-          const uint4* src = reinterpret_cast<const uint4*>(p.q + row_id * p.D + d0);
+          const uint4* src = reinterpret_cast<const uint4*>(p.q + row_id * p.Dqk + d0);
           for (int cq = half * (C::DH / 16); cq < (half + 1) * (C::DH / 16); ++cq) {
             uint4 v = make_uint4(0, 0, 0, 0);
             if (row_valid) v = src[cq];
@@ -1041,8 +1044,8 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
         if (__any_sync(0xffffffffu, rescale_o)) {
           const float a = rescale_o ? alpha : 1.f;
 #pragma unroll 1
-          for (int cch = 0; cch < C::DH / 64; ++cch) {
-            const uint32_t col = half * (C::DH / 2) + cch * 32;
+          for (int cch = 0; cch < C::DV / 64; ++cch) {
+            const uint32_t col = half * (C::DV / 2) + cch * 32;
             uint32_t r[32];
             ptx::tmem_ld32(lane_base + col, r);
             ptx::tmem_wait_ld();
@@ -1100,8 +1103,8 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
         }
         if (count > 0) {
 #pragma unroll 1
-          for (int cch = 0; cch < C::DH / 64; ++cch) {
-            const int col = half * (C::DH / 2) + cch * 32;
+          for (int cch = 0; cch < C::DV / 64; ++cch) {
+            const int col = half * (C::DV / 2) + cch * 32;
             uint32_t r[32];
             ptx::tmem_ld32(lane_base + col, r);
             ptx::tmem_wait_ld();
@@ -1122,8 +1125,8 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
         const long long sr = sk_row(pc.slot);
         if (half == 0) reinterpret_cast<float2*>(p.sk_ml)[sr] = make_float2(m_run, l);
 #pragma unroll 1
-        for (int cch = 0; cch < C::DH / 64; ++cch) {
-          const int col = half * (C::DH / 2) + cch * 32;
+        for (int cch = 0; cch < C::DV / 64; ++cch) {
+          const int col = half * (C::DV / 2) + cch * 32;
           uint32_t r[32];
           ptx::tmem_ld32(lane_base + col, r);
           ptx::tmem_wait_ld();
@@ -1178,8 +1181,8 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
         }
         const float inv = ltot > 0.f ? 1.f / ltot : 0.f;
 #pragma unroll 1
-        for (int cch = 0; cch < C::DH / 64; ++cch) {
-          const int col = half * (C::DH / 2) + cch * 32;
+        for (int cch = 0; cch < C::DV / 64; ++cch) {
+          const int col = half * (C::DV / 2) + cch * 32;
           uint32_t r[32];
           ptx::tmem_ld32(lane_base + col, r);
           ptx::tmem_wait_ld();

@@ -142,37 +142,49 @@ int sdpa_decode(const void* q, const void* k, const void* v, void* out, int B, i
 size_t sdpa_decode_workspace_bytes(int B, int Hq, int Hkv, int Lq, int D);
 
 /*
- * K/V read from a caller's cache instead of packed [B, Hkv, Lk, D] tensors.
+ * Extended prefill / decode: a V head dim that differs from Q/K's, and K/V read
+ * from a caller's cache instead of packed tensors.
  *
- * The pages' serving code decodes against KV caches: classic decode and the
- * per-row verify calls read "strided, sliced keys", and sliding-window layers
- * keep their keys in a ring addressed by a cursor ("fix: Gemma 4 MTP never
- * engages on CUDA (GB10), verify probe fails", sections "Current Behavior"
- * and "Proposed Solution"; a wrapped ring and an unwrapped one are both edge
- * cases in "Implementation Notes").
+ * Head dims.  q and k have Dqk columns, v and out have Dv.  Supported: Dqk ==
+ * Dv in {128, 192, 256, 512}, and Dqk = 192 with Dv = 256, the Q=192/K=192/
+ * V=256 heads that "Fused SDPA full-attention for head_dim=192/256" (MLX PR
+ * #3660, thread under "Additional head dimension discovered") names as gated
+ * out of the fused path.  Scores are q.k over Dqk; out is the weighted sum of
+ * V rows over Dv.  Workspace sizes: sdpa_prefill_workspace_bytes with Dqk,
+ * sdpa_decode_workspace_bytes with Dv.
  *
- * k, v  [B, Hkv, kv_capacity, D] contiguous, same dtype as q; only the rows
- *       below are read.
- * kv_ring = 0: key j (0 <= j < Lk) is row j; kv_capacity >= Lk.
- * kv_ring = 1: key j is row (j mod kv_capacity): the cache holds the last
- *       kv_capacity keys.  kv_capacity must be a multiple of 128 and hold every
- *       key some query row can see: min(Lk, Lq + window - 1) keys with a window,
- *       all Lk keys without one.  Rows of the ring that no query row can see
- *       are read but weighted by exactly 0; they must hold finite values.
- * Everything else is as for sdpa_prefill / sdpa_decode (same workspace sizes);
- * the results equal, bit for bit, the calls on packed copies of the same keys,
- * so decode row invariance holds over the trimmed prefix of the same cache.
- * Layout errors return SDPA_ERR_INVALID_ARG before anything is queued.
+ * K/V caches.  The pages' serving code decodes against KV caches: classic
+ * decode and the per-row verify calls read "strided, sliced keys", and
+ * sliding-window layers keep their keys in a ring addressed by a cursor ("fix:
+ * Gemma 4 MTP never engages on CUDA (GB10), verify probe fails", sections
+ * "Current Behavior" and "Proposed Solution"; a wrapped ring and an unwrapped
+ * one are both edge cases in "Implementation Notes").
+ *  k  [B, Hkv, kv_capacity, Dqk], v [B, Hkv, kv_capacity, Dv], contiguous,
+ *     same dtype as q; only the rows below are read.
+ *  kv_ring = 0: key j (0 <= j < Lk) is row j; kv_capacity >= Lk (kv_capacity
+ *     = Lk is the packed layout of sdpa_prefill / sdpa_decode).
+ *  kv_ring = 1: key j is row (j mod kv_capacity): the cache holds the last
+ *     kv_capacity keys.  kv_capacity must be a multiple of 128 and hold every
+ *     key some query row can see: min(Lk, Lq + window - 1) keys with a window,
+ *     all Lk keys without one.  Rows of the ring that no query row can see are
+ *     read but weighted by exactly 0; they must hold finite values.
+ * The layout changes only which row holds a key: results equal, bit for bit,
+ * the same call on packed copies of the keys, so decode row invariance holds
+ * over the trimmed prefix of the same cache.
+ *
+ * Everything else is as for sdpa_prefill / sdpa_decode.  Unsupported head dims
+ * return SDPA_ERR_UNSUPPORTED and layout errors SDPA_ERR_INVALID_ARG before
+ * anything is queued.
  */
-int sdpa_prefill_kv(const void* q, const void* k, const void* v, void* out, int B, int Hq,
-                    int Hkv, int Lq, int Lk, int D, float scale, int causal, int window,
+int sdpa_prefill_ex(const void* q, const void* k, const void* v, void* out, int B, int Hq,
+                    int Hkv, int Lq, int Lk, int Dqk, int Dv, float scale, int causal, int window,
                     int dtype, int kv_capacity, int kv_ring, void* workspace,
                     size_t workspace_bytes, sdpa_stream_t stream);
 
-int sdpa_decode_kv(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
-                   int Lq, int Lk, int D, float scale, int causal, int window, int dtype,
-                   int kv_capacity, int kv_ring, void* workspace, size_t workspace_bytes,
-                   sdpa_stream_t stream);
+int sdpa_decode_ex(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
+                   int Lq, int Lk, int Dqk, int Dv, float scale, int causal, int window,
+                   int dtype, int kv_capacity, int kv_ring, void* workspace,
+                   size_t workspace_bytes, sdpa_stream_t stream);
 
 /* Synchronises `stream`, returns SDPA_OK or SDPA_ERR_DEVICE_TIMEOUT for the
  * current device and clears the status word.  *detail (if not NULL) receives

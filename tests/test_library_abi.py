@@ -91,19 +91,25 @@ def test_launch_query_rejects_bad_arguments_on_the_host(lib):
     assert lib.sdpa_prefill_launches(1, 2, 1, 9, 8, 256, 1, 0, 0) == -1   # causal Lq > Lk
 
 
-def call_kv(lib, fn, cap, ring, Lq=4, Lk=3000, window=1024, causal=1):
-    return getattr(lib, fn)(FAKE, FAKE, FAKE, FAKE, 1, 2, 1, Lq, Lk, 256, 0.0625, causal, window,
-                            0, cap, ring, FAKE, 1 << 20, None)
+def call_ex(lib, fn, cap, ring, Lq=4, Lk=3000, window=1024, causal=1, Dqk=256, Dv=256):
+    return getattr(lib, fn)(FAKE, FAKE, FAKE, FAKE, 1, 2, 1, Lq, Lk, Dqk, Dv, 0.0625, causal,
+                            window, 0, cap, ring, FAKE, 1 << 20, None)
 
 
-@pytest.mark.parametrize("fn", ["sdpa_prefill_kv", "sdpa_decode_kv"])
+@pytest.mark.parametrize("fn", ["sdpa_prefill_ex", "sdpa_decode_ex"])
 def test_cache_layouts_are_checked_on_the_host(lib, fn):
-    assert call_kv(lib, fn, 2000, 0) == -1          # packed cache shorter than Lk
-    assert call_kv(lib, fn, 1000, 1) == -1          # ring not a multiple of 128
-    assert call_kv(lib, fn, 896, 1) == -1           # ring misses keys the window sees
-    assert call_kv(lib, fn, 4096, 2) == -1          # ring flag not 0/1
-    assert call_kv(lib, fn, 0, 0) == -1
-    assert call_kv(lib, fn, 2048, 1, window=0) == -1  # no window: the ring must hold all Lk
+    assert call_ex(lib, fn, 2000, 0) == -1          # packed cache shorter than Lk
+    assert call_ex(lib, fn, 1000, 1) == -1          # ring not a multiple of 128
+    assert call_ex(lib, fn, 896, 1) == -1           # ring misses keys the window sees
+    assert call_ex(lib, fn, 4096, 2) == -1          # ring flag not 0/1
+    assert call_ex(lib, fn, 0, 0) == -1
+    assert call_ex(lib, fn, 2048, 1, window=0) == -1  # no window: the ring must hold all Lk
+
+
+@pytest.mark.parametrize("fn", ["sdpa_prefill_ex", "sdpa_decode_ex"])
+def test_unequal_head_dims_are_checked_on_the_host(lib, fn):
+    for dqk, dv in ((256, 128), (128, 256), (192, 128), (512, 256), (256, 192)):
+        assert call_ex(lib, fn, 3000, 0, Dqk=dqk, Dv=dv) == -2, (dqk, dv)
 
 
 def test_missing_library_fails_loudly(tmp_path):

@@ -117,6 +117,21 @@ def test_matches_numpy_brute_force(case):
     assert np.max(np.abs(got - ref)) < 1e-12
 
 
+@pytest.mark.parametrize("dims", [(128, 128), (192, 192), (192, 256)])
+def test_other_head_dims_match_torch_and_brute_force(dims):
+    """Head dims 128 and 192, and Q/K 192 with V 256: scores over Dqk columns,
+    output over Dv, against both independent references."""
+    D, Dv = dims
+    q, k, v = rand_qkv(1, 4, 2, 13, 29, D, torch.float16, seed=D + Dv, Dv=Dv)
+    scale = 1.0 / math.sqrt(D)
+    for causal, window in ((True, 0), (True, 7), (False, 0)):
+        got = oracle.sdpa(q, k, v, scale=scale, causal=causal, window=window)
+        assert got.shape == (1, 4, 13, Dv)
+        ref = torch_reference(q, k, v, scale, causal, window).numpy()
+        assert np.max(np.abs(got - ref)) < 1e-12
+        assert np.max(np.abs(got - numpy_dense(q, k, v, scale, causal, window))) < 1e-12
+
+
 def test_two_key_worked_example():
     gold = json.load(open(os.path.join(GOLDEN, "two_key_softmax.json")))
     D = 256
