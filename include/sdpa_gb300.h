@@ -138,7 +138,8 @@ int sdpa_decode(const void* q, const void* k, const void* v, void* out, int B, i
                 int Lq, int Lk, int D, float scale, int causal, int window, int dtype,
                 void* workspace, size_t workspace_bytes, sdpa_stream_t stream);
 
-/* Workspace bytes sdpa_decode needs on the current device (0 on bad arguments). */
+/* Workspace bytes sdpa_decode needs on the current device (0 on bad arguments);
+ * enough for any window (a windowed call splits its keys into fewer pieces). */
 size_t sdpa_decode_workspace_bytes(int B, int Hq, int Hkv, int Lq, int D);
 
 /*
