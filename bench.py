@@ -330,6 +330,57 @@ def profile_run(args):
     return 0 if st[0] == 0 else 1
 
 
+# ---------------------------------------------------------------- routing study
+
+def routing_study():
+    """The pages route kL <= 16384 to an unfused path (matmul, softmax, matmul)
+    because their fused kernel lost there ("Fused SDPA full-attention for
+    head_dim=192/256", the routing discussion under "Microbenchmarks").  Here:
+    the fused call against that unfused path built from torch (cuBLAS GEMMs, a
+    dense mask and softmax), at the long-KV GQA head geometry, queries at the
+    end of the keys, for kL from 512 to 16384.  Measurement only."""
+    import attention_sm_flash_attn_gb300 as gb
+    from attention_sm_flash_attn_gb300 import build as gbbuild
+    gbbuild.build()
+    device = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    flush = L2Flush(device)
+    rows = []
+    for kL in (512, 1024, 2048, 4096, 8192, 16384):
+        w = wl.LONGKV.with_(Lq=min(1024, kL), Lk=kL)
+        q, k, v = wl.make_qkv(w, device=device)
+        out = torch.empty_like(q)
+        nb = gb.prefill_workspace_bytes(w.B, w.Hq, w.Hkv, w.Lq, w.Lk, w.D, True, 0)
+        ws = torch.empty(max(1, nb), dtype=torch.uint8, device=device)
+        G = w.Hq // w.Hkv
+        i = torch.arange(w.Lq, device=device).view(-1, 1) + (w.Lk - w.Lq)
+        visible = torch.arange(w.Lk, device=device).view(1, -1) <= i
+
+        def fused():
+            gb.sdpa_prefill(q, k, v, out, scale=w.scale, causal=True, workspace=ws)
+
+        def unfused():
+            kk = k.repeat_interleave(G, dim=1)
+            vv = v.repeat_interleave(G, dim=1)
+            s = torch.matmul(q, kk.transpose(-1, -2)).float() * w.scale
+            s.masked_fill_(~visible, float("-inf"))
+            p = torch.softmax(s, dim=-1).to(q.dtype)
+            return torch.matmul(p, vv)
+
+        err = float((unfused().float() - (fused() or out).float()).abs().max())
+        tf = statistics.median(time_calls(fused, 10, 3, flush, stream))
+        tu = statistics.median(time_calls(unfused, 10, 3, flush, stream))
+        rows.append({"kL": kL, "qL": w.Lq, "fused_ms": round(tf, 4), "unfused_ms": round(tu, 4),
+                     "unfused_over_fused": round(tu / tf, 2),
+                     "fused_tflops": round(prefill_flops(w) / tf / 1e9, 1),
+                     "max_abs_diff": round(err, 5)})
+        del q, k, v, out, ws, visible
+        torch.cuda.empty_cache()
+    print(json.dumps({"routing_study": "fused vs unfused prefill, Hq=16, Hkv=8, D=256, fp16, "
+                                       "bottom-right causal", "rows": rows}), flush=True)
+    return 0
+
+
 # ---------------------------------------------------------------- ranks
 
 def max_over_ranks(value: float, dist, device) -> float:
@@ -397,9 +448,14 @@ def main():
     ap.add_argument("--profile", default=None,
                     help="run one named workload --steps times (for ncu) and exit; decode "
                          "workloads take a _LqN suffix")
+    ap.add_argument("--routing", action="store_true",
+                    help="fused vs unfused (cuBLAS matmul + softmax + matmul) prefill time over "
+                         "kL, one JSON line, and exit")
     args = ap.parse_args()
     if args.profile:
         return profile_run(args)
+    if args.routing:
+        return routing_study()
     args.warmup = max(3, args.warmup)
     world, rank, local, dist = dist_setup(args)
     if args.impl == "reference":
