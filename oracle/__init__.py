@@ -58,6 +58,12 @@ def _load():
                                     c_int, c_int, c_int, c_double, c_int, c_int,
                                     ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, c_int]
         lib.oracle_sdpa.restype = c_int
+        i64 = ctypes.c_int64
+        lib.oracle_sdpa_bias.argtypes = [u16p, u16p, u16p, u16p, i64, i64, i64, c_int, c_int,
+                                         c_int, c_int, c_int, c_int, c_int, c_int, c_double,
+                                         c_int, c_int, ctypes.c_void_p, ctypes.c_int64,
+                                         ctypes.c_void_p, c_int]
+        lib.oracle_sdpa_bias.restype = c_int
         lib.oracle_row_scores.argtypes = [u16p, u16p, c_int, c_int, c_int, c_int, c_int,
                                           c_int, c_int, c_double, c_int, c_int, c_int,
                                           ctypes.c_void_p]
@@ -89,13 +95,16 @@ def max_threads() -> int:
 
 
 def sdpa(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: float | None = None,
-         causal: bool = False, window: int = 0, rows=None, nthreads: int = 0) -> np.ndarray:
+         causal: bool = False, window: int = 0, rows=None, nthreads: int = 0,
+         bias: torch.Tensor | None = None) -> np.ndarray:
     """Exact-input fp64 attention.
 
     q: [B, Hq, Lq, Dqk], k: [B, Hkv, Lk, Dqk], v: [B, Hkv, Lk, Dv], all fp16 or all
     bf16 (CPU or GPU tensors; they are copied to host).  ``rows`` is None (every
     row; result shaped [B, Hq, Lq, Dv]) or an iterable of flat row ids
-    ``(b * Hq + h) * Lq + i`` (result shaped [len(rows), Dv]).
+    ``(b * Hq + h) * Lq + i`` (result shaped [len(rows), Dv]).  ``bias`` (same
+    dtype, shape [B or 1, Hq or 1, Lq or 1, Lk]) is added to the scaled scores;
+    -inf removes a key, and a row left without keys outputs zeros.
     """
     if not (q.dtype == k.dtype == v.dtype):
         raise TypeError("q, k, v must share one dtype")
@@ -116,10 +125,27 @@ def sdpa(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: float | No
         ids = np.ascontiguousarray(np.asarray(list(rows), dtype=np.int64))
         n = ids.shape[0]
     out = np.zeros((n, Dv), dtype=np.float64)
-    rc = _load().oracle_sdpa(
-        qn.ctypes.data, kn.ctypes.data, vn.ctypes.data, _dtype_code(q), B, Hq, Hkv, Lq, Lk,
-        Dqk, Dv, float(scale), int(bool(causal)), int(window),
-        None if ids is None else ids.ctypes.data, n, out.ctypes.data, int(nthreads))
+    if bias is None:
+        rc = _load().oracle_sdpa(
+            qn.ctypes.data, kn.ctypes.data, vn.ctypes.data, _dtype_code(q), B, Hq, Hkv, Lq, Lk,
+            Dqk, Dv, float(scale), int(bool(causal)), int(window),
+            None if ids is None else ids.ctypes.data, n, out.ctypes.data, int(nthreads))
+    else:
+        if bias.dtype != q.dtype or bias.dim() != 4 or bias.shape[3] != Lk:
+            raise ValueError("bias must be [B or 1, Hq or 1, Lq or 1, Lk] in q's dtype")
+        b0, h0, q0 = bias.shape[:3]
+        if b0 not in (1, B) or h0 not in (1, Hq) or q0 not in (1, Lq):
+            raise ValueError("bias must broadcast to [B, Hq, Lq, Lk]")
+        bt, bn = _as_u16(bias)
+        sb = 0 if b0 == 1 else h0 * q0 * Lk
+        sh = 0 if h0 == 1 else q0 * Lk
+        sq = 0 if q0 == 1 else Lk
+        rc = _load().oracle_sdpa_bias(
+            qn.ctypes.data, kn.ctypes.data, vn.ctypes.data, bn.ctypes.data, sb, sh, sq,
+            _dtype_code(q), B, Hq, Hkv, Lq, Lk, Dqk, Dv, float(scale), int(bool(causal)),
+            int(window), None if ids is None else ids.ctypes.data, n, out.ctypes.data,
+            int(nthreads))
+        del bt
     if rc != 0:
         raise ValueError(f"oracle_sdpa rejected the call (status {rc})")
     del qt, kt, vt

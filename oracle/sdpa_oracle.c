@@ -13,6 +13,7 @@
  *     p_i  = Lk - Lq + i                                      (bottom-right position)
  *     V_i  = { j in [0, Lk) : (!causal or j <= p_i) and (W == 0 or p_i - j < W) }
  *     s_j  = scale * sum_d q[b,h,i,d] * k[b,g,j,d]            (exact fp16/bf16 -> double)
+ *            [+ bias[b,h,i,j] when an additive bias (mask array) is given]
  *     P_j  = exp(s_j - max_{V_i} s) / sum_{V_i} exp(s - max s)     for j in V_i, else 0
  *     o[b,h,i,:] = sum_j P_j * v[b,g,j,:]
  *
@@ -37,7 +38,9 @@
  * bottom-right; a window W keeps the W keys j with p_i - j < W (the query's
  * own key included); W = 0 means no window; a window requires causal; query
  * head h reads KV head floor(h / G).  Masked keys are excluded (weight 0), not
- * given a large negative additive value.
+ * given a large negative additive value.  An additive bias is added after the
+ * scale (as the dense additive mask of mlxcel issue #672 is); a bias entry of
+ * -inf removes a key, and a row left with no key outputs zeros.
  */
 #include <math.h>
 #include <stdint.h>
@@ -100,7 +103,7 @@ static int check_args(int B, int Hq, int Hkv, int Lq, int Lk, int Dqk, int Dv,
 static void row_scores(const uint16_t *q, const uint16_t *k, int dtype, int Hq, int Hkv,
                        int Lq, int Lk, int Dqk, double scale, int b, int h, int i,
                        int only_visible, int causal, int window, double *qrow,
-                       double *s) {
+                       double *s, const uint16_t *brow) {
   int G = Hq / Hkv;
   int g = h / G;
   const int64_t qoff = (((int64_t)b * Hq + h) * Lq + i) * Dqk;
@@ -112,11 +115,12 @@ static void row_scores(const uint16_t *q, const uint16_t *k, int dtype, int Hq, 
     double acc = 0.0;
     for (int d = 0; d < Dqk; ++d) acc += qrow[d] * elem(k, kbase + j * Dqk + d, dtype);
     s[j] = scale * acc;
+    if (brow) s[j] += elem(brow, j, dtype); /* additive bias (mask array) entry */
   }
 }
 
 /* Step 2: softmax over the visible set; P_j = 0 outside it.  Returns -2 if the
- * visible set is empty. */
+ * visible set is empty, 1 (all P_j = 0) if a bias gave every visible key -inf. */
 static int row_probs(const double *s, int Lq, int Lk, int i, int causal, int window,
                      double *P) {
   int64_t p = (int64_t)Lk - Lq + i;
@@ -128,6 +132,10 @@ static int row_probs(const double *s, int Lq, int Lk, int i, int causal, int win
       if (s[j] > mx) mx = s[j];
     }
   if (!any) return -2;
+  if (mx == -INFINITY) {
+    for (int64_t j = 0; j < Lk; ++j) P[j] = 0.0;
+    return 1;
+  }
   double den = 0.0;
   for (int64_t j = 0; j < Lk; ++j) {
     P[j] = visible(j, p, causal, window) ? exp(s[j] - mx) : 0.0;
@@ -158,7 +166,7 @@ int oracle_row_scores(const uint16_t *q, const uint16_t *k, int dtype, int B, in
   if (b < 0 || b >= B || h < 0 || h >= Hq || i < 0 || i >= Lq) return -1;
   double *qrow = (double *)malloc(sizeof(double) * (size_t)Dqk);
   if (!qrow) return -3;
-  row_scores(q, k, dtype, Hq, Hkv, Lq, Lk, Dqk, scale, b, h, i, 0, 0, 0, qrow, s_out);
+  row_scores(q, k, dtype, Hq, Hkv, Lq, Lk, Dqk, scale, b, h, i, 0, 0, 0, qrow, s_out, NULL);
   free(qrow);
   return 0;
 }
@@ -173,7 +181,8 @@ int oracle_row_probs(const uint16_t *q, const uint16_t *k, int dtype, int B, int
   double *qrow = (double *)malloc(sizeof(double) * (size_t)Dqk);
   int rc = -3;
   if (s && qrow) {
-    row_scores(q, k, dtype, Hq, Hkv, Lq, Lk, Dqk, scale, b, h, i, 0, causal, window, qrow, s);
+    row_scores(q, k, dtype, Hq, Hkv, Lq, Lk, Dqk, scale, b, h, i, 0, causal, window, qrow, s,
+               NULL);
     rc = row_probs(s, Lq, Lk, i, causal, window, p_out);
   }
   free(s);
@@ -188,10 +197,11 @@ int oracle_row_probs(const uint16_t *q, const uint16_t *k, int dtype, int B, int
  * nthreads <= 0 lets OpenMP choose.  Returns 0, -1 (bad argument),
  * -2 (a row with no visible key) or -3 (out of memory).
  */
-int oracle_sdpa(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
-                int B, int Hq, int Hkv, int Lq, int Lk, int Dqk, int Dv, double scale,
-                int causal, int window, const int64_t *row_ids, int64_t n_rows,
-                double *out, int nthreads) {
+static int sdpa_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     const uint16_t *bias, int64_t sb, int64_t sh, int64_t sq, int dtype,
+                     int B, int Hq, int Hkv, int Lq, int Lk, int Dqk, int Dv, double scale,
+                     int causal, int window, const int64_t *row_ids, int64_t n_rows,
+                     double *out, int nthreads) {
   if (check_args(B, Hq, Hkv, Lq, Lk, Dqk, Dv, causal, window, dtype)) return -1;
   const int64_t total = (int64_t)B * Hq * Lq;
   if (n_rows < 0 || (!row_ids && n_rows != total)) return -1;
@@ -222,8 +232,11 @@ int oracle_sdpa(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dty
       int i = (int)(id % Lq);
       int h = (int)((id / Lq) % Hq);
       int b = (int)(id / ((int64_t)Lq * Hq));
-      row_scores(q, k, dtype, Hq, Hkv, Lq, Lk, Dqk, scale, b, h, i, 1, causal, window, qrow, s);
-      if (row_probs(s, Lq, Lk, i, causal, window, P)) {
+      const uint16_t *brow = bias ? bias + b * sb + h * sh + i * sq : NULL;
+      row_scores(q, k, dtype, Hq, Hkv, Lq, Lk, Dqk, scale, b, h, i, 1, causal, window, qrow, s,
+                 brow);
+      int pr = row_probs(s, Lq, Lk, i, causal, window, P);
+      if (pr < 0) {
 #ifdef _OPENMP
 #pragma omp atomic write
 #endif
@@ -237,6 +250,30 @@ int oracle_sdpa(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dty
     free(qrow);
   }
   return status;
+}
+
+int oracle_sdpa(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
+                int B, int Hq, int Hkv, int Lq, int Lk, int Dqk, int Dv, double scale,
+                int causal, int window, const int64_t *row_ids, int64_t n_rows,
+                double *out, int nthreads) {
+  return sdpa_rows(q, k, v, NULL, 0, 0, 0, dtype, B, Hq, Hkv, Lq, Lk, Dqk, Dv, scale, causal,
+                   window, row_ids, n_rows, out, nthreads);
+}
+
+/*
+ * The same with an additive bias (a mask array): s_j += bias[b*sb + h*sh + i*sq
+ * + j], the bias in q's dtype (strides in elements; 0 broadcasts over batch or
+ * head).  A bias entry of -inf removes the key; a row whose visible keys all
+ * get -inf outputs zeros.
+ */
+int oracle_sdpa_bias(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     const uint16_t *bias, int64_t sb, int64_t sh, int64_t sq, int dtype, int B,
+                     int Hq, int Hkv, int Lq, int Lk, int Dqk, int Dv, double scale, int causal,
+                     int window, const int64_t *row_ids, int64_t n_rows, double *out,
+                     int nthreads) {
+  if (!bias || sb < 0 || sh < 0 || sq < 0) return -1;
+  return sdpa_rows(q, k, v, bias, sb, sh, sq, dtype, B, Hq, Hkv, Lq, Lk, Dqk, Dv, scale, causal,
+                   window, row_ids, n_rows, out, nthreads);
 }
 
 /* The thread count OpenMP would use (1 without OpenMP). */

@@ -28,6 +28,10 @@ MUTANTS = {
     "bf16_truncated_mantissa": ("uint32_t bits = (uint32_t)b << 16;", "uint32_t bits = (uint32_t)(b & 0xFFF0) << 16;"),
     "softmax_not_normalised": ("for (int64_t j = 0; j < Lk; ++j) P[j] /= den;", "(void)den;"),
     "scale_dropped": ("s[j] = scale * acc;", "s[j] = acc;"),
+    "bias_subtracted": ("if (brow) s[j] += elem(", "if (brow) s[j] -= elem("),
+    "bias_scaled": ("if (brow) s[j] += elem(brow, j, dtype);",
+                    "if (brow) s[j] += scale * elem(brow, j, dtype);"),
+    "bias_head_stride_ignored": ("bias + b * sb + h * sh + i * sq", "bias + b * sb + i * sq"),
 }
 
 PIN_CHECKS = [
@@ -41,6 +45,8 @@ PIN_CHECKS = [
     lambda: pins.test_input_widening_is_exact(torch.bfloat16),
     lambda: pins.test_probability_rows_sum_to_one(True, 5),
     lambda: pins.test_two_key_worked_example(),
+    lambda: pins.test_log_weight_bias_with_zero_query_gives_weighted_mean(),
+    lambda: pins.test_bias_matches_torch_sdpa_float_mask((2, 4, 9), torch.float16),
 ]
 
 
@@ -61,7 +67,8 @@ def test_mutant_is_caught(name, tmp_path, monkeypatch):
     real = oracle._load()
     so = _build_mutant(tmp_path, name, *MUTANTS[name])
     lib = ctypes.CDLL(so)
-    for fn in ("oracle_sdpa", "oracle_row_scores", "oracle_row_probs", "oracle_max_threads"):
+    for fn in ("oracle_sdpa", "oracle_sdpa_bias", "oracle_row_scores", "oracle_row_probs",
+               "oracle_max_threads"):
         getattr(lib, fn).argtypes = getattr(real, fn).argtypes
         getattr(lib, fn).restype = getattr(real, fn).restype
     monkeypatch.setattr(oracle, "_lib", lib)

@@ -359,3 +359,148 @@ def test_workload_shapes_reproduce_the_pages_input_sizes():
         assert (w.Hq, w.Hkv, w.D) == (hd["n_q"], hd["n_kv"], hd["head_dim"])
     assert (LONGKV.Lq, LONGKV.Lk) == (gold["rows"][0]["qL"], gold["rows"][0]["kL"])
     assert (PREFILL128K.Lq, PREFILL128K.Lk) == (gold["rows"][2]["qL"], gold["rows"][2]["kL"])
+
+
+# --- additive bias (mask array) ------------------------------------------------
+# "fix: gemma-4 long-prompt prefill OOMs on CUDA" (mlxcel issue #672, sections
+# "Root cause" and "Suggested fix direction") describes the model handing SDPA a
+# dense additive mask (0 for a visible key, -inf for a hidden one) and cuDNN's
+# flash path taking such a mask as a bias.  The bias is added to the scaled
+# scores; a row whose keys are all hidden outputs zeros.
+
+BIAS_SHAPES = [(1, 1, 1), (2, 1, 1), (1, 4, 1), (1, 1, 9), (2, 4, 9)]
+
+
+def rand_bias(shape, Lk, dtype, seed, hide=0.3):
+    """Finite N(0, 2) entries with about ``hide`` of them -inf."""
+    g = torch.Generator().manual_seed(seed)
+    b = torch.randn(*shape, Lk, generator=g) * 2.0
+    b[torch.rand(*shape, Lk, generator=g) < hide] = -math.inf
+    return b.to(dtype)
+
+
+def torch_bias_reference(q, k, v, scale, causal, window, bias):
+    """torch's SDPA in float64 with a float mask: the bias plus -inf where the
+    causal / window flags hide a key; rows left without keys are zeros."""
+    G = q.shape[1] // k.shape[1]
+    kk = k.double().repeat_interleave(G, dim=1)
+    vv = v.double().repeat_interleave(G, dim=1)
+    m = mask_matrix(q.shape[2], k.shape[2], causal, window)
+    add = bias.double().expand(q.shape[0], q.shape[1], q.shape[2], k.shape[2]).clone()
+    add = add.masked_fill(~m, -math.inf)
+    out = F.scaled_dot_product_attention(q.double(), kk, vv, attn_mask=add, scale=scale)
+    empty = torch.isinf(add).all(dim=-1, keepdim=True)
+    return out.masked_fill(empty, 0.0)
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("shape", BIAS_SHAPES)
+def test_bias_matches_torch_sdpa_float_mask(shape, dtype):
+    B, Hq, Hkv, Lq, Lk, D = 2, 4, 2, 9, 40, 256
+    q, k, v = rand_qkv(B, Hq, Hkv, Lq, Lk, D, dtype, seed=31)
+    bias = rand_bias(shape, Lk, dtype, seed=sum(shape))
+    scale = 1.0 / math.sqrt(D)
+    for causal, window in ((False, 0), (True, 0), (True, 5)):
+        got = oracle.sdpa(q, k, v, scale=scale, causal=causal, window=window, bias=bias)
+        ref = torch_bias_reference(q, k, v, scale, causal, window, bias).numpy()
+        assert np.max(np.abs(got - ref)) < 1e-12, (causal, window)
+
+
+def test_bias_matches_numpy_brute_force():
+    """Dense scores plus the bias element by element, softmax by hand."""
+    B, Hq, Hkv, Lq, Lk, D, Dv = 1, 2, 1, 6, 11, 192, 256
+    q, k, v = rand_qkv(B, Hq, Hkv, Lq, Lk, D, torch.bfloat16, seed=33, Dv=Dv)
+    bias = rand_bias((B, Hq, Lq), Lk, torch.bfloat16, seed=34, hide=0.2)
+    bias[0, 1, 2, :] = -math.inf          # one row with every key hidden
+    scale = 0.07
+    got = oracle.sdpa(q, k, v, scale=scale, causal=False, bias=bias)
+    qn, kn, vn, bn = (x.double().numpy() for x in (q, k, v, bias))
+    for h in range(Hq):
+        for i in range(Lq):
+            s = [scale * float(np.dot(qn[0, h, i], kn[0, 0, j])) + bn[0, h, i, j]
+                 for j in range(Lk)]
+            if all(x == -math.inf for x in s):
+                want = np.zeros(Dv)
+            else:
+                mx = max(s)
+                e = [math.exp(x - mx) for x in s]
+                want = sum(e[j] * vn[0, 0, j] for j in range(Lk)) / sum(e)
+            assert np.max(np.abs(got[0, h, i] - want)) < 1e-12, (h, i)
+
+
+def test_zero_bias_equals_no_bias_exactly():
+    q, k, v = rand_qkv(1, 4, 2, 17, 60, 256, torch.float16, seed=35)
+    for causal, window in ((False, 0), (True, 0), (True, 9)):
+        a = oracle.sdpa(q, k, v, causal=causal, window=window)
+        z = torch.zeros(1, 1, 1, 60, dtype=torch.float16)
+        assert np.array_equal(a, oracle.sdpa(q, k, v, causal=causal, window=window, bias=z))
+
+
+@pytest.mark.parametrize("window", [0, 7])
+def test_inf_bias_pattern_equals_the_mask_flags(window):
+    """A 0/-inf bias holding the bottom-right causal (and window) pattern, on a
+    call without flags, gives the flagged call's result exactly."""
+    Lq, Lk = 13, 50
+    q, k, v = rand_qkv(1, 2, 1, Lq, Lk, 256, torch.bfloat16, seed=36)
+    m = mask_matrix(Lq, Lk, True, window)
+    bias = torch.zeros(1, 1, Lq, Lk).masked_fill(~m, -math.inf).to(torch.bfloat16)
+    want = oracle.sdpa(q, k, v, causal=True, window=window)
+    assert np.array_equal(oracle.sdpa(q, k, v, causal=False, bias=bias), want)
+
+
+def test_row_constant_bias_cancels():
+    """Softmax is invariant to a constant added across a row: a bias constant
+    along keys (different per head and row) leaves the result unchanged."""
+    q, k, v = rand_qkv(1, 4, 2, 8, 30, 256, torch.float16, seed=37)
+    c = torch.tensor([0.5, -3.0, 8.0, 1.25]).view(1, 4, 1, 1) * torch.ones(1, 4, 8, 30)
+    c = c + torch.arange(8).view(1, 1, 8, 1) * 0.25
+    a = oracle.sdpa(q, k, v, causal=True)
+    b = oracle.sdpa(q, k, v, causal=True, bias=c.to(torch.float16))
+    assert np.max(np.abs(a - b)) < 1e-12
+
+
+def test_log_weight_bias_with_zero_query_gives_weighted_mean():
+    """With q = 0 every score is the bias, so a bias of log w_j makes the output
+    the w-weighted mean of the values: sum_j w_j v_j / sum_j w_j."""
+    Lk, D = 24, 256
+    _, k, v = rand_qkv(1, 1, 1, 1, Lk, D, torch.float16, seed=38)
+    q = torch.zeros(1, 1, 1, D, dtype=torch.float16)
+    logw = torch.linspace(-2.0, 2.0, Lk).to(torch.float16)
+    w = np.exp(logw.double().numpy())
+    got = oracle.sdpa(q, k, v, causal=False, bias=logw.view(1, 1, 1, Lk))
+    want = (w[:, None] * v[0, 0].double().numpy()).sum(0) / w.sum()
+    assert np.max(np.abs(got[0, 0, 0] - want)) < 1e-12
+
+
+def test_fully_hidden_rows_output_zeros():
+    q, k, v = rand_qkv(1, 2, 1, 4, 10, 256, torch.float16, seed=39)
+    bias = torch.zeros(1, 2, 4, 10, dtype=torch.float16)
+    bias[0, 0, 1] = -math.inf
+    bias[0, 1, 3, 5:] = -math.inf        # with causal, row 3 sees keys 0..9; keep 0..4
+    bias[0, 1, 0, :7] = -math.inf        # row 0 sees keys 0..6 under causal: all hidden
+    got = oracle.sdpa(q, k, v, causal=True, bias=bias)
+    assert np.all(got[0, 0, 1] == 0.0) and np.all(got[0, 1, 0] == 0.0)
+    assert np.any(got[0, 1, 3] != 0.0)
+
+
+def test_bias_rows_subset_matches_full_call():
+    q, k, v = rand_qkv(2, 4, 2, 7, 33, 256, torch.bfloat16, seed=40)
+    bias = rand_bias((2, 1, 7), 33, torch.bfloat16, seed=41)
+    full = oracle.sdpa(q, k, v, causal=True, window=4, bias=bias).reshape(-1, 256)
+    ids = np.array([0, 5, 13, 27, 55], dtype=np.int64)
+    assert np.array_equal(oracle.sdpa(q, k, v, causal=True, window=4, bias=bias, rows=ids),
+                          full[ids])
+
+
+@pytest.mark.parametrize("bad", [(1, 1, 1, 39), (3, 1, 1, 40), (1, 3, 1, 40), (1, 1, 2, 40),
+                                 (1, 40)])
+def test_rejects_bias_that_does_not_broadcast(bad):
+    q, k, v = rand_qkv(2, 4, 2, 9, 40, 256, torch.float16, seed=42)
+    with pytest.raises(ValueError):
+        oracle.sdpa(q, k, v, bias=torch.zeros(*bad, dtype=torch.float16))
+
+
+def test_rejects_bias_of_another_dtype():
+    q, k, v = rand_qkv(1, 2, 1, 4, 8, 256, torch.float16, seed=43)
+    with pytest.raises(ValueError):
+        oracle.sdpa(q, k, v, bias=torch.zeros(1, 1, 1, 8, dtype=torch.bfloat16))
