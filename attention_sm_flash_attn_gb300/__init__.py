@@ -61,8 +61,10 @@ def load_library(path: str | None = None):
         lib.sdpa_prefill.restype = i
         lib.sdpa_decode.argtypes = attn
         lib.sdpa_decode.restype = i
-        # ..., Lk, Dqk, Dv, scale, causal, window, dtype, kv_capacity, kv_ring, ws, bytes, stream
-        attn_ex = attn[:10] + [i] + attn[10:14] + [i, i] + attn[14:]
+        # ..., Lk, Dqk, Dv, scale, causal, window, dtype, kv_capacity, kv_ring,
+        # bias, bias strides (b, h, q), ws, bytes, stream
+        ll = ctypes.c_longlong
+        attn_ex = attn[:10] + [i] + attn[10:14] + [i, i, vp, ll, ll, ll] + attn[14:]
         lib.sdpa_prefill_ex.argtypes = attn_ex
         lib.sdpa_prefill_ex.restype = i
         lib.sdpa_decode_ex.argtypes = attn_ex
@@ -159,19 +161,40 @@ def _workspace(nbytes: int, device, workspace):
     return workspace
 
 
+def _bias_args(bias, q, B, Hq, Lq, Lk):
+    """(pointer, stride_b, stride_h, stride_q) of a bias broadcastable to [B, Hq,
+    Lq, Lk]; size-1 dims broadcast (stride 0), the key dim must be dense."""
+    if bias is None:
+        return None, 0, 0, 0
+    if not bias.is_cuda or bias.device != q.device:
+        raise ValueError("bias must be a CUDA tensor on q's device")
+    if bias.dtype != q.dtype:
+        raise TypeError("bias must have q's dtype")
+    if bias.dim() != 4 or bias.shape[3] != Lk:
+        raise ValueError("bias must be 4-D [B or 1, Hq or 1, Lq or 1, Lk]")
+    for n, full in zip(bias.shape[:3], (B, Hq, Lq)):
+        if n not in (1, full):
+            raise ValueError("bias must broadcast to [B, Hq, Lq, Lk]")
+    if Lk > 1 and bias.stride(3) != 1:
+        raise ValueError("bias rows must be contiguous along keys")
+    st = [0 if bias.shape[d] == 1 else bias.stride(d) for d in range(3)]
+    return bias.data_ptr(), st[0], st[1], st[2]
+
+
 def _call(entry, ex_entry, q, k, v, out, B, Hq, Hkv, Lq, Lk, D, Dv, scale, causal, window, lk,
-          ring, workspace, stream):
+          ring, workspace, stream, bias=None):
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
     lib = load_library()
     head = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, Hq, Hkv, Lq, Lk, D)
     tail = (float(scale), int(bool(causal)), int(window), _dtype_code(q))
-    if lk is None and not ring and Dv == D:
+    bias_ptr, sb, sh, sq = _bias_args(bias, q, B, Hq, Lq, Lk)
+    if lk is None and not ring and Dv == D and bias is None:
         rc = getattr(lib, entry)(*head, *tail, ws_ptr, ws_len, _stream_ptr(stream))
         name = entry
     else:
-        rc = getattr(lib, ex_entry)(*head, Dv, *tail, int(k.shape[2]), int(bool(ring)), ws_ptr,
-                                    ws_len, _stream_ptr(stream))
+        rc = getattr(lib, ex_entry)(*head, Dv, *tail, int(k.shape[2]), int(bool(ring)), bias_ptr,
+                                    sb, sh, sq, ws_ptr, ws_len, _stream_ptr(stream))
         name = ex_entry
     if rc != 0:
         raise SdpaError(rc, name)
@@ -185,13 +208,14 @@ def _out(q, v, out):
 
 
 def sdpa_prefill(q, k, v, out=None, *, scale=None, causal=False, window=0, workspace=None,
-                 stream=None, lk=None, ring=False):
+                 stream=None, lk=None, ring=False, bias=None):
     """Fused attention over [B, H, L, D] fp16/bf16 CUDA tensors (see sdpa_prefill and
     sdpa_prefill_ex in include/sdpa_gb300.h).  Returns ``out``.  ``workspace`` may
     be a uint8 CUDA tensor; when None one is allocated with torch if the schedule
     wants it.  v may have its own head dim (Q/K 192 with V 256).  With ``lk``
     given (or ``ring``), k and v are a K/V cache of k.shape[2] rows holding
-    Lk = lk keys."""
+    Lk = lk keys.  ``bias`` (q's dtype, [B or 1, Hq or 1, Lq or 1, Lk], dense along
+    keys) is added to the scaled scores; -inf hides a key."""
     out = _out(q, v, out)
     B, Hq, Hkv, Lq, Lk, D, Dv = _check(q, k, v, out, lk)
     if scale is None:
@@ -199,14 +223,14 @@ def sdpa_prefill(q, k, v, out=None, *, scale=None, causal=False, window=0, works
     need = prefill_workspace_bytes(B, Hq, Hkv, Lq, Lk, D, causal, window)
     workspace = _workspace(need, q.device, workspace)
     return _call("sdpa_prefill", "sdpa_prefill_ex", q, k, v, out, B, Hq, Hkv, Lq, Lk, D, Dv,
-                 scale, causal, window, lk, ring, workspace, stream)
+                 scale, causal, window, lk, ring, workspace, stream, bias)
 
 
 def sdpa_decode(q, k, v, out=None, *, scale=None, causal=True, window=0, workspace=None,
-                stream=None, lk=None, ring=False):
+                stream=None, lk=None, ring=False, bias=None):
     """Split-KV decode / verify for 1 <= Lq <= 8 (see sdpa_decode and sdpa_decode_ex
-    in include/sdpa_gb300.h).  Returns ``out``.  Head dims, ``lk`` and ``ring`` as
-    for sdpa_prefill."""
+    in include/sdpa_gb300.h).  Returns ``out``.  Head dims, ``lk``, ``ring`` and
+    ``bias`` as for sdpa_prefill."""
     out = _out(q, v, out)
     B, Hq, Hkv, Lq, Lk, D, Dv = _check(q, k, v, out, lk)
     if scale is None:
@@ -214,7 +238,7 @@ def sdpa_decode(q, k, v, out=None, *, scale=None, causal=True, window=0, workspa
     need = decode_workspace_bytes(B, Hq, Hkv, Lq, Dv)
     workspace = _workspace(need, q.device, workspace)
     return _call("sdpa_decode", "sdpa_decode_ex", q, k, v, out, B, Hq, Hkv, Lq, Lk, D, Dv,
-                 scale, causal, window, lk, ring, workspace, stream)
+                 scale, causal, window, lk, ring, workspace, stream, bias)
 
 
 def device_status(stream=None):

@@ -43,25 +43,52 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(s) <= t for s in _sources())
 
 
-def compile_command(out: str):
+def _flags():
+    return [ARCH, "-O3", "-std=c++17", "-lineinfo", "-Xptxas", "-v", "-Xcompiler", "-fPIC",
+            "-I", INCLUDE]
+
+
+def compile_commands(out: str):
+    """One `nvcc -c` per translation unit (run in parallel), then the link."""
     nvcc = _nvcc()
     cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nvcc)), "lib64")
-    return [nvcc, ARCH, "-O3", "-std=c++17", "-lineinfo", "-Xptxas", "-v",
-            "-Xcompiler", "-fPIC", "-shared", "-cudart", "shared",
-            f"-Xlinker", f"-rpath,{cuda_lib}",
-            "-I", INCLUDE, "-o", out, os.path.join(CSRC, "sdpa_api.cu")]
+    obj_dir = os.path.join(HERE, "_build")
+    units = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    objs = [os.path.join(obj_dir, os.path.basename(u)[:-3] + f".{os.getpid()}.o") for u in units]
+    compiles = [[nvcc, *_flags(), "-c", u, "-o", o] for u, o in zip(units, objs)]
+    link = [nvcc, ARCH, "-shared", "-cudart", "shared", "-Xlinker", f"-rpath,{cuda_lib}",
+            "-o", out, *objs]
+    return compiles, link, objs
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
     if not force and up_to_date():
         return LIB_PATH
     tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = compile_command(tmp)
-    res = subprocess.run(cmd, capture_output=True, text=True)
-    if res.returncode != 0:
-        raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + res.stdout + res.stderr)
+    compiles, link, objs = compile_commands(tmp)
+    os.makedirs(os.path.join(HERE, "_build"), exist_ok=True)
+    log = []
+    try:
+        procs = [(c, subprocess.Popen(c, stdout=subprocess.PIPE, stderr=subprocess.STDOUT,
+                                      text=True)) for c in compiles]
+        failed = None
+        for c, pr in procs:
+            out, _ = pr.communicate()
+            log.append(out)
+            if pr.returncode != 0 and failed is None:
+                failed = (c, out)
+        if failed:
+            raise RuntimeError("nvcc failed:\n" + " ".join(failed[0]) + "\n" + failed[1])
+        res = subprocess.run(link, capture_output=True, text=True)
+        log.append(res.stdout + res.stderr)
+        if res.returncode != 0:
+            raise RuntimeError("link failed:\n" + " ".join(link) + "\n" + res.stdout + res.stderr)
+    finally:
+        for o in objs:
+            if os.path.exists(o):
+                os.remove(o)
     if verbose:
-        print(res.stdout + res.stderr)
+        print("".join(log))
     os.replace(tmp, LIB_PATH)
     return LIB_PATH
 

@@ -13,25 +13,18 @@
 #include <mutex>
 
 #include "sdpa_gb300.h"
-#include "sdpa_kernels.cuh"
+#include "sdpa_launch.cuh"
 
 namespace {
 
 using gbsdpa::AttnParams;
 using gbsdpa::Cfg;
+using gbsdpa_host::DeviceState;
 
 __device__ int g_device_status;
 
 constexpr int kMaxDevices = 64;
 
-struct DeviceState {
-  bool ready = false;
-  int sms = 0;
-  int* status = nullptr;  // device address of g_device_status
-  bool attr_set[32] = {};   // per kernel instantiation (variant_index)
-  int sk_units[32] = {};    // resident persistent units per instantiation
-  unsigned long long epoch = 0;          // last persistent-launch epoch handed out
-};
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
@@ -111,8 +104,6 @@ int validate(const void* q, const void* k, const void* v, const void* out, int B
   return SDPA_OK;
 }
 
-// Slot of a kernel instantiation in the per-device tables: dtype x variant x
-// per-CTA head dim (256, 128, 192).
 // K/V in a cache of kv_cap rows per (b, kv head): packed rows 0..Lk-1
 // (kv_cap >= Lk), or a ring where key j sits in row j mod kv_cap.  A ring must
 // hold every key some row can see (the window plus the query rows, or all Lk
@@ -121,6 +112,22 @@ int validate(const void* q, const void* k, const void* v, const void* out, int B
 int validate_dims(int Dqk, int Dv) {
   if (Dqk == Dv) return SDPA_OK;  // checked with the rest of the arguments
   return (Dqk == 192 && Dv == 256) ? SDPA_OK : SDPA_ERR_UNSUPPORTED;
+}
+
+// Additive bias: entry (b, h, i, j) at ptr[b * sb + h * sh + i * sq + j], in q's
+// dtype; strides are elements, >= 0 (0 broadcasts).  Null ptr: no bias.
+struct BiasArg {
+  const void* ptr = nullptr;
+  long long sb = 0, sh = 0, sq = 0;
+};
+
+int validate_bias(const BiasArg& b) {
+  if (!b.ptr) return SDPA_OK;
+  const long long lim = 1ll << 48;
+  if (b.sb < 0 || b.sh < 0 || b.sq < 0 || b.sb > lim || b.sh > lim || b.sq > lim)
+    return SDPA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(b.ptr) & 1u) return SDPA_ERR_ALIGNMENT;
+  return SDPA_OK;
 }
 
 int validate_kv_layout(int Lq, int Lk, int causal, int window, int kv_cap, int kv_ring) {
@@ -132,100 +139,6 @@ int validate_kv_layout(int Lq, int Lk, int causal, int window, int kv_cap, int k
                              ? std::min<long long>(Lk, static_cast<long long>(Lq) + window - 1)
                              : Lk;
   return span <= kv_cap ? SDPA_OK : SDPA_ERR_INVALID_ARG;
-}
-
-// Slot of a kernel instantiation in the per-device tables: dtype x variant x
-// per-CTA head dims (Q/K, V): (256, 256), (128, 128), (192, 192), (192, 256).
-template <bool BF16, int MODE, int HD, int HDV>
-constexpr int variant_index() {
-  return (BF16 ? 1 : 0) +
-         2 * (MODE * 4 + (HD != HDV ? 3 : HD == 256 ? 0 : HD == 128 ? 1 : 2));
-}
-constexpr int kNumVariants = 2 * 4 * 4;
-static_assert(sizeof(DeviceState::attr_set) == kNumVariants * sizeof(bool) &&
-                  sizeof(DeviceState::sk_units) == kNumVariants * sizeof(int),
-              "one table entry per kernel instantiation");
-static_assert(variant_index<false, gbsdpa::kSingle, 192, 256>() !=
-                  variant_index<false, gbsdpa::kSingle, 192, 192>(),
-              "distinct slots");
-
-template <bool BF16, int MODE, int HD, int HDV>
-int ensure_attr(DeviceState* st) {
-  const int idx = variant_index<BF16, MODE, HD, HDV>();
-  if (st->attr_set[idx]) return SDPA_OK;
-  auto kern = gbsdpa::attn_fwd_kernel<BF16, MODE, HD, HDV>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg<BF16, MODE, HD, HDV>::SMEM_BYTES) != cudaSuccess)
-    return SDPA_ERR_CUDA;
-  st->attr_set[idx] = true;
-  return SDPA_OK;
-}
-
-template <bool BF16, int MODE, int HD, int HDV>
-void fill_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, long long ctas,
-                 cudaStream_t stream) {
-  constexpr bool kCluster = MODE != gbsdpa::kSingle;
-  *cfg = {};
-  cfg->gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
-  cfg->blockDim = dim3(Cfg<BF16, MODE, HD, HDV>::NTHREADS, 1, 1);
-  cfg->dynamicSmemBytes = Cfg<BF16, MODE, HD, HDV>::SMEM_BYTES;
-  cfg->stream = stream;
-  cfg->attrs = attr;
-  cfg->numAttrs = 0;
-  if (kCluster) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg->numAttrs = 1;
-  }
-}
-
-template <bool BF16, int MODE, int HD, int HDV>
-int launch_attn(const AttnParams& p, long long items, cudaStream_t stream, DeviceState* st) {
-  int rc = ensure_attr<BF16, MODE, HD, HDV>(st);
-  if (rc) return rc;
-  constexpr bool kCluster = MODE != gbsdpa::kSingle;
-  const long long ctas = items * (kCluster ? 2 : 1);
-  if (ctas <= 0 || ctas > 0x7fffffffll) return SDPA_ERR_INVALID_ARG;
-  cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[1];
-  // A persistent grid waits on itself (prefix units on suffix units).  It is
-  // sized to the occupancy limit, so on an otherwise idle GPU all of it is
-  // resident; the kernel starts the never-waiting units first, and a wait that
-  // still runs out reports a device timeout instead of hanging.
-  fill_launch<BF16, MODE, HD, HDV>(&cfg, attr, ctas, stream);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gbsdpa::attn_fwd_kernel<BF16, MODE, HD, HDV>, p);
-  return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
-}
-
-// How many persistent units (CTAs, or CTA pairs for the 2-SM variant) can be
-// resident at once on this device; 0 if the variant cannot run persistently.
-template <bool BF16, int MODE, int HD, int HDV>
-int resident_units(DeviceState* st) {
-  const int idx = variant_index<BF16, MODE, HD, HDV>();
-  if (st->sk_units[idx]) return st->sk_units[idx];
-  if (ensure_attr<BF16, MODE, HD, HDV>(st)) return 0;
-  int units = 0;
-  if (MODE == gbsdpa::kSingle) {
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gbsdpa::attn_fwd_kernel<BF16, MODE, HD, HDV>,
-                                                      Cfg<BF16, MODE, HD, HDV>::NTHREADS,
-                                                      Cfg<BF16, MODE, HD, HDV>::SMEM_BYTES) != cudaSuccess)
-      return 0;
-    units = per_sm * st->sms;
-  } else {
-    cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
-    fill_launch<BF16, MODE, HD, HDV>(&cfg, attr, 2 * (st->sms / 2), nullptr);
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, gbsdpa::attn_fwd_kernel<BF16, MODE, HD, HDV>, &cfg) !=
-        cudaSuccess)
-      return 0;
-    units = clusters;
-  }
-  st->sk_units[idx] = std::max(0, units);
-  return st->sk_units[idx];
 }
 
 int launch_combine(const float* part_o, const float* part_ml, void* out, long long R, int D,
@@ -425,19 +338,10 @@ TailPlan plan_tail(long long units, int B, int Hq, int Lq, int Lk, int causal, i
 // Units for a persistent prefill launch (0: one CTA per query tile instead).
 template <bool BF16>
 long long persistent_units(DeviceState* st, int mode, int D, int B, int Hq, int Lq, int Lk,
-                           int causal, int window, int Dv = 0) {
+                           int causal, int window, int Dv = 0, bool bias = false) {
   if (Dv <= 0) Dv = D;
-  int units = 0;
-  if (mode == gbsdpa::kSingle) {
-    units = D != Dv    ? resident_units<BF16, gbsdpa::kSingle, 192, 256>(st)
-            : D == 128 ? resident_units<BF16, gbsdpa::kSingle, 128, 128>(st)
-            : D == 192 ? resident_units<BF16, gbsdpa::kSingle, 192, 192>(st)
-                       : resident_units<BF16, gbsdpa::kSingle, 256, 256>(st);
-  } else if (mode == gbsdpa::kDuo) {
-    units = D == 128 ? resident_units<BF16, gbsdpa::kDuo, 128, 128>(st)
-                     : resident_units<BF16, gbsdpa::kDuo, 256, 256>(st);
-  }
-  else return 0;
+  const int units = bias ? gbsdpa_host::resident_bias_variant(BF16, mode, D, Dv, st)
+                         : gbsdpa_host::resident_variant<BF16, false>(mode, D, Dv, st);
   if (units <= 0) return 0;
   const long long W =
       total_key_tiles(B, Hq, Lq, Lk, causal, window, key_tile(mode), qtile_rows(mode));
@@ -448,7 +352,8 @@ template <bool BF16>
 int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv, int Lq,
         int Lk, int D, float scale, int causal, int window, bool decode, int n_splits,
         bool write_partial, void* workspace, cudaStream_t stream, DeviceState* st,
-        int withhold_q = 0, long long sk_units = 0, int kv_cap = 0, int kv_ring = 0, int Dv = 0) {
+        int withhold_q = 0, long long sk_units = 0, int kv_cap = 0, int kv_ring = 0, int Dv = 0,
+        const BiasArg& bias = BiasArg()) {
   // D is the Q/K head dim; Dv (0: the same) is V's and the output's.
   if (Dv <= 0) Dv = D;
   AttnParams p;
@@ -494,6 +399,13 @@ int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, i
   // scale == 0 becomes a tiny c, for which every visible weight is exactly 1.
   p.c = std::max(static_cast<float>(static_cast<double>(scale) * 1.4426950408889634), 1e-30f);
   p.decode = decode ? 1 : 0;
+  if (bias.ptr) {
+    p.bias = static_cast<const uint16_t*>(bias.ptr);
+    p.bias_sb = bias.sb;
+    p.bias_sh = bias.sh;
+    p.bias_sq = bias.sq;
+    p.bias_vec = aligned16(bias.ptr) && bias.sb % 8 == 0 && bias.sh % 8 == 0 && bias.sq % 8 == 0;
+  }
   p.n_qtiles = (Lq + qtile_rows(mode) - 1) / qtile_rows(mode);
   p.n_splits = n_splits;
   p.n_hb = (p.G + 15) / 16;
@@ -522,19 +434,8 @@ int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, i
     items = static_cast<long long>(B) * Hkv * n_splits * p.n_hb;
   else
     items = static_cast<long long>(B) * Hq * p.n_qtiles * n_splits;
-  switch (mode) {
-    case gbsdpa::kPair: rc = launch_attn<BF16, gbsdpa::kPair, 256, 256>(p, items, stream, st); break;
-    case gbsdpa::kDuo:
-      rc = D == 128 ? launch_attn<BF16, gbsdpa::kDuo, 128, 128>(p, items, stream, st)
-                    : launch_attn<BF16, gbsdpa::kDuo, 256, 256>(p, items, stream, st);
-      break;
-    default:
-      rc = D != Dv    ? launch_attn<BF16, gbsdpa::kSingle, 192, 256>(p, items, stream, st)
-           : D == 128 ? launch_attn<BF16, gbsdpa::kSingle, 128, 128>(p, items, stream, st)
-           : D == 192 ? launch_attn<BF16, gbsdpa::kSingle, 192, 192>(p, items, stream, st)
-                      : launch_attn<BF16, gbsdpa::kSingle, 256, 256>(p, items, stream, st);
-      break;
-  }
+  rc = p.bias ? gbsdpa_host::launch_bias_variant(BF16, mode, D, Dv, p, items, stream, st)
+              : gbsdpa_host::launch_variant<BF16, false>(mode, D, Dv, p, items, stream, st);
   if (rc) return rc;
   if (write_partial)
     rc = launch_combine(p.part_o, p.part_ml, out, R, Dv, n_splits, BF16, stream);
@@ -592,12 +493,15 @@ size_t sdpa_decode_workspace_bytes(int B, int Hq, int Hkv, int Lq, int D) {
 static int prefill_impl(const void* q, const void* k, const void* v, void* out, int B, int Hq,
                         int Hkv, int Lq, int Lk, int D, int Dv, float scale, int causal,
                         int window, int dtype, int kv_cap, int kv_ring, void* workspace,
-                        size_t workspace_bytes, sdpa_stream_t stream) {
+                        size_t workspace_bytes, sdpa_stream_t stream,
+                        const BiasArg& bias = BiasArg()) {
   int rc = validate(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, dtype);
   if (rc) return rc;
   rc = validate_dims(D, Dv);
   if (rc) return rc;
   rc = validate_kv_layout(Lq, Lk, causal, window, kv_cap, kv_ring);
+  if (rc) return rc;
+  rc = validate_bias(bias);
   if (rc) return rc;
   if (workspace && !aligned16(workspace)) return SDPA_ERR_ALIGNMENT;
   DeviceState* st = nullptr;
@@ -606,32 +510,37 @@ static int prefill_impl(const void* q, const void* k, const void* v, void* out, 
   const bool bf16 = dtype == SDPA_BF16;
   auto strm = reinterpret_cast<cudaStream_t>(stream);
   const int mode = choose_mode(false, D, window);
-  const long long u = bf16 ? persistent_units<true>(st, mode, D, B, Hq, Lq, Lk, causal, window, Dv)
-                           : persistent_units<false>(st, mode, D, B, Hq, Lq, Lk, causal, window, Dv);
+  const bool has_bias = bias.ptr != nullptr;
+  const long long u =
+      bf16 ? persistent_units<true>(st, mode, D, B, Hq, Lq, Lk, causal, window, Dv, has_bias)
+           : persistent_units<false>(st, mode, D, B, Hq, Lq, Lk, causal, window, Dv, has_bias);
   if (u > 0 && workspace && workspace_bytes >= sk_layout(u).bytes)
     return bf16 ? run<true>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, false, 1,
-                            false, workspace, strm, st, 0, u, kv_cap, kv_ring, Dv)
+                            false, workspace, strm, st, 0, u, kv_cap, kv_ring, Dv, bias)
                 : run<false>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, false, 1,
-                             false, workspace, strm, st, 0, u, kv_cap, kv_ring, Dv);
+                             false, workspace, strm, st, 0, u, kv_cap, kv_ring, Dv, bias);
   int s = u > 0 ? 1 : plan_prefill_splits(st->sms, B, Hq, Lq, Lk, D, causal, window);
   if (s > 1 && (!workspace ||
                 workspace_bytes < partial_bytes(static_cast<long long>(B) * Hq * Lq, Dv, s)))
     s = 1;
   return bf16 ? run<true>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, false, s,
-                          s > 1, workspace, strm, st, 0, 0, kv_cap, kv_ring, Dv)
+                          s > 1, workspace, strm, st, 0, 0, kv_cap, kv_ring, Dv, bias)
               : run<false>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, false, s,
-                           s > 1, workspace, strm, st, 0, 0, kv_cap, kv_ring, Dv);
+                           s > 1, workspace, strm, st, 0, 0, kv_cap, kv_ring, Dv, bias);
 }
 
 static int decode_impl(const void* q, const void* k, const void* v, void* out, int B, int Hq,
                        int Hkv, int Lq, int Lk, int D, int Dv, float scale, int causal,
                        int window, int dtype, int kv_cap, int kv_ring, void* workspace,
-                       size_t workspace_bytes, sdpa_stream_t stream) {
+                       size_t workspace_bytes, sdpa_stream_t stream,
+                       const BiasArg& bias = BiasArg()) {
   int rc = validate(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, dtype);
   if (rc) return rc;
   rc = validate_dims(D, Dv);
   if (rc) return rc;
   rc = validate_kv_layout(Lq, Lk, causal, window, kv_cap, kv_ring);
+  if (rc) return rc;
+  rc = validate_bias(bias);
   if (rc) return rc;
   if (Lq > 8) return SDPA_ERR_INVALID_ARG;
   if (!workspace) return SDPA_ERR_WORKSPACE;
@@ -645,9 +554,9 @@ static int decode_impl(const void* q, const void* k, const void* v, void* out, i
   const bool bf16 = dtype == SDPA_BF16;
   auto strm = reinterpret_cast<cudaStream_t>(stream);
   return bf16 ? run<true>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, true, s,
-                          true, workspace, strm, st, 0, 0, kv_cap, kv_ring, Dv)
+                          true, workspace, strm, st, 0, 0, kv_cap, kv_ring, Dv, bias)
               : run<false>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, true, s,
-                           true, workspace, strm, st, 0, 0, kv_cap, kv_ring, Dv);
+                           true, workspace, strm, st, 0, 0, kv_cap, kv_ring, Dv, bias);
 }
 
 int sdpa_prefill(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
@@ -666,18 +575,30 @@ int sdpa_decode(const void* q, const void* k, const void* v, void* out, int B, i
 
 int sdpa_prefill_ex(const void* q, const void* k, const void* v, void* out, int B, int Hq,
                     int Hkv, int Lq, int Lk, int Dqk, int Dv, float scale, int causal, int window,
-                    int dtype, int kv_capacity, int kv_ring, void* workspace,
-                    size_t workspace_bytes, sdpa_stream_t stream) {
+                    int dtype, int kv_capacity, int kv_ring, const void* bias,
+                    long long bias_stride_b, long long bias_stride_h, long long bias_stride_q,
+                    void* workspace, size_t workspace_bytes, sdpa_stream_t stream) {
+  BiasArg b;
+  b.ptr = bias;
+  b.sb = bias_stride_b;
+  b.sh = bias_stride_h;
+  b.sq = bias_stride_q;
   return prefill_impl(q, k, v, out, B, Hq, Hkv, Lq, Lk, Dqk, Dv, scale, causal, window, dtype,
-                      kv_capacity, kv_ring, workspace, workspace_bytes, stream);
+                      kv_capacity, kv_ring, workspace, workspace_bytes, stream, b);
 }
 
 int sdpa_decode_ex(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
                    int Lq, int Lk, int Dqk, int Dv, float scale, int causal, int window,
-                   int dtype, int kv_capacity, int kv_ring, void* workspace,
-                   size_t workspace_bytes, sdpa_stream_t stream) {
+                   int dtype, int kv_capacity, int kv_ring, const void* bias,
+                   long long bias_stride_b, long long bias_stride_h, long long bias_stride_q,
+                   void* workspace, size_t workspace_bytes, sdpa_stream_t stream) {
+  BiasArg b;
+  b.ptr = bias;
+  b.sb = bias_stride_b;
+  b.sh = bias_stride_h;
+  b.sq = bias_stride_q;
   return decode_impl(q, k, v, out, B, Hq, Hkv, Lq, Lk, Dqk, Dv, scale, causal, window, dtype,
-                     kv_capacity, kv_ring, workspace, workspace_bytes, stream);
+                     kv_capacity, kv_ring, workspace, workspace_bytes, stream, b);
 }
 
 int sdpa_device_status(sdpa_stream_t stream, int* detail) {

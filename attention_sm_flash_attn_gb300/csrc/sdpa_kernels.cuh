@@ -104,6 +104,14 @@ struct AttnParams {
   float* sk_ml;                // [n_units][2][128][2]
   unsigned long long* sk_flag; // [n_units][2]
   unsigned long long epoch;
+  // Additive bias (a mask array), or null: entry (b, h, i, j) at
+  // bias[b * bias_sb + h * bias_sh + i * bias_sq + j] (elements, q's dtype; a
+  // stride of 0 broadcasts), added to the scaled score of query row i and key j.
+  // bias_vec = 1: base and strides are 16-byte multiples, so a row is read in
+  // 8-element vectors.
+  const uint16_t* bias;
+  long long bias_sb, bias_sh, bias_sq;
+  int bias_vec;
 };
 
 // Kernel variants.
@@ -459,6 +467,38 @@ __device__ __forceinline__ bool iter_next(const AttnParams& p, IterState& st, Pi
   return false;
 }
 
+// Bias entries for keys [k0, k0 + N) of one row, as N / 2 packed 16-bit pairs;
+// keys at or past Lk (masked anyway) and rows without a bias (brow null) read 0.
+template <int N>
+__device__ __forceinline__ void load_bias(const uint16_t* brow, int k0, int Lk, bool vec,
+                                          uint32_t (&bw)[N / 2]) {
+#pragma unroll
+  for (int c = 0; c < N / 8; ++c) {
+    const int kc = k0 + 8 * c;
+    if (brow != nullptr && vec && kc + 8 <= Lk) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(brow + kc));
+      bw[4 * c] = u.x;
+      bw[4 * c + 1] = u.y;
+      bw[4 * c + 2] = u.z;
+      bw[4 * c + 3] = u.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const uint32_t lo = (brow != nullptr && kc + e < Lk) ? __ldg(brow + kc + e) : 0u;
+        const uint32_t hi = (brow != nullptr && kc + e + 1 < Lk) ? __ldg(brow + kc + e + 1) : 0u;
+        bw[4 * c + e / 2] = lo | (hi << 16);
+      }
+    }
+  }
+}
+
+// The two 16-bit values of a packed pair, widened (exactly) to float.
+__device__ __forceinline__ float2 unpack2(uint32_t w, bool bf16) {
+  if (bf16) return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  __half2 h = *reinterpret_cast<__half2*>(&w);
+  return __half22float2(h);
+}
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
   if (bf16) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -469,7 +509,9 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
   }
 }
 
-template <bool BF16, int MODE, int HD, int HDV>
+// BIAS: add the caller's additive bias (p.bias) to the scores; the kernels
+// without it never read p.bias.
+template <bool BF16, int MODE, int HD, int HDV, bool BIAS = false>
 __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
   using C = Cfg<BF16, MODE, HD, HDV>;
   constexpr bool PAIR = C::PAIR;
@@ -803,6 +845,8 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
     };
 
     const float c = p.c;
+    const float cs = BIAS ? 1.f : c;  // factor from the scores held in s to log2 units
+    constexpr float kLog2e = 1.4426950408889634f;
     bool ok = true;      // false once the two halves of this row pair agree to stop
     bool alive = true;   // false once a wait of this warp gave up
     int use = 0;  // pair-barrier uses so far
@@ -840,11 +884,14 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
       int row_p;            // bottom-right position of this row
       bool row_valid;
       long long row_id;     // flat (b, h, i) row index, -1 if none
+      const uint16_t* brow = nullptr;  // this row's bias entries (key 0), if any
       if (!p.decode) {
         const int i = w.m0 + t;
         row_valid = i < p.Lq;
         row_p = p.Lk - p.Lq + min(i, p.Lq - 1);
         row_id = row_valid ? (static_cast<long long>(w.b) * p.Hq + w.h0) * p.Lq + i : -1;
+        if (BIAS && row_valid)
+          brow = p.bias + w.b * p.bias_sb + w.h0 * p.bias_sh + i * p.bias_sq;
       } else {
         const int hl = t >> 3;
         const int slot = t & 7;
@@ -854,6 +901,8 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
         row_valid = (i < p.Lq) && (hl < min(p.G, 16)) && (h < (w.hkv + 1) * p.G);
         row_p = base + (row_valid ? i : 0);
         row_id = row_valid ? (static_cast<long long>(w.b) * p.Hq + h) * p.Lq + i : -1;
+        if (BIAS && row_valid)
+          brow = p.bias + w.b * p.bias_sb + h * p.bias_sh + i * p.bias_sq;
         if (count > 0) {
           // Decode: stage this thread's half of the row's query slice into the
           // swizzled Q tile (16-byte chunks of 8 elements).
@@ -904,10 +953,38 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
         float s[HB];
 #pragma unroll
         for (int e = 0; e < HB; ++e) s[e] = -INFINITY;
+        // Bias: this tile's entries are requested before the wait for S, and the
+        // next tile's lines are prefetched into L2.
+        uint32_t bw[BIAS ? HB / 2 : 1];
+        if constexpr (BIAS) {
+          load_bias<HB>(brow, kb, p.Lk, p.bias_vec != 0, bw);
+          if (brow != nullptr && j + 1 < count) {
+            const int kn = (tile + w.t_step) * BN + half * HB;
+            if (kn < p.Lk) ptx::prefetch_l2(brow + kn);
+            if (kn + HB - 1 < p.Lk) ptx::prefetch_l2(brow + kn + HB - 1);
+          }
+        }
         if (alive)
           alive = __all_sync(0xffffffffu, wait_bar(bar(kBarSFull + buf), (gt >> 1) & 1,
                                                    abort_flag, p.status, kDevTimeoutSFull));
-        if (alive) {
+        if (BIAS && !PAIR && alive) {
+          // Scores straight to the log2 domain, c * s + log2(e) * bias, one
+          // 32-column chunk at a time (a masked key becomes -inf below).
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int cch = 0; cch < HB / 32; ++cch) {
+            uint32_t r[32];
+            ptx::tmem_ld32(lane_base + C::S_COL + buf * BN + half * HB + cch * 32, r);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence(r);
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float2 bv = unpack2(bw[(cch * 32 + e) / 2], BF16);
+              s[cch * 32 + e] = fmaf(__uint_as_float(r[e]), c, bv.x * kLog2e);
+              s[cch * 32 + e + 1] = fmaf(__uint_as_float(r[e + 1]), c, bv.y * kLog2e);
+            }
+          }
+        } else if (alive) {
           ptx::tc_fence_after();
           uint32_t r[HB / 32][32];
 #pragma unroll
@@ -992,6 +1069,16 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
             s[e] = vis ? s[e] : -INFINITY;
           }
         }
+        // Pair with a bias: the summed scores move to the log2 domain here (-inf,
+        // from the mask or the bias, stays -inf).  With a bias cs = 1 below.
+        if constexpr (BIAS && PAIR) {
+#pragma unroll
+          for (int e = 0; e < HB; e += 2) {
+            const float2 bv = unpack2(bw[e / 2], BF16);
+            s[e] = fmaf(s[e], c, bv.x * kLog2e);
+            s[e + 1] = fmaf(s[e + 1], c, bv.y * kLog2e);
+          }
+        }
         // Row max: tree over this half, then swap with the other half.
         float mh;
         {
@@ -1006,7 +1093,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
         float mo;
         ok = swap_half(mh, mo);
         if (!ok) break;  // both halves of the row stop together
-        const float xm = fmaxf(mh, mo) * c;  // c > 0, so -inf stays -inf
+        const float xm = fmaxf(mh, mo) * cs;  // cs > 0, so -inf stays -inf
         const bool grow = xm > m_run + 8.0f;
         const float m_old = m_run;
         const bool rescale_o = grow && (m_old != -INFINITY) && (j > 0);
@@ -1018,15 +1105,15 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
         }
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
 
-        // Probabilities 2^(c*s - m), partial row sum, pack to 16-bit pairs.
+        // Probabilities 2^(cs*s - m), partial row sum, pack to 16-bit pairs.
         uint32_t pk[HB / 2];
         float ls[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) ls[k] = 0.f;
 #pragma unroll
         for (int e = 0; e < HB; e += 2) {
-          const float p0 = ptx::ex2(fmaf(s[e], c, -m_use));
-          const float p1 = ptx::ex2(fmaf(s[e + 1], c, -m_use));
+          const float p0 = ptx::ex2(fmaf(s[e], cs, -m_use));
+          const float p1 = ptx::ex2(fmaf(s[e + 1], cs, -m_use));
           ls[(e >> 1) & 7] += p0 + p1;
           pk[e / 2] = pack2(p0, p1, BF16);
         }

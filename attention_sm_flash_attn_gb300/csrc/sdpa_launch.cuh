@@ -1,0 +1,167 @@
+// sdpa_launch.cuh -- per-device launch state and the launch of one attention
+// kernel instantiation, shared by the translation units that instantiate them:
+// sdpa_api.cu (kernels without a bias) and sdpa_bias.cu (kernels that add an
+// additive bias to the scores).  Splitting the instantiations over two units
+// lets them compile in parallel.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "sdpa_gb300.h"
+#include "sdpa_kernels.cuh"
+
+namespace gbsdpa_host {
+
+using gbsdpa::AttnParams;
+using gbsdpa::Cfg;
+
+// Slot of a kernel instantiation in the per-device tables: bias x dtype x
+// variant x per-CTA head dims (Q/K, V): (256, 256), (128, 128), (192, 192),
+// (192, 256).
+template <bool BF16, int MODE, int HD, int HDV, bool BIAS>
+constexpr int variant_index() {
+  return (BIAS ? 32 : 0) + (BF16 ? 1 : 0) +
+         2 * (MODE * 4 + (HD != HDV ? 3 : HD == 256 ? 0 : HD == 128 ? 1 : 2));
+}
+constexpr int kNumVariants = 2 * 2 * 4 * 4;
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  int* status = nullptr;                // device address of the status word
+  bool attr_set[kNumVariants] = {};     // per kernel instantiation (variant_index)
+  int sk_units[kNumVariants] = {};      // resident persistent units per instantiation
+  unsigned long long epoch = 0;         // last persistent-launch epoch handed out
+};
+
+static_assert(variant_index<false, gbsdpa::kSingle, 192, 256, false>() !=
+                      variant_index<false, gbsdpa::kSingle, 192, 192, false>() &&
+                  variant_index<true, gbsdpa::kDuo, 256, 256, true>() < kNumVariants,
+              "distinct slots within the tables");
+
+template <bool BF16, int MODE, int HD, int HDV, bool BIAS>
+int ensure_attr(DeviceState* st) {
+  constexpr int idx = variant_index<BF16, MODE, HD, HDV, BIAS>();
+  if (st->attr_set[idx]) return SDPA_OK;
+  auto kern = gbsdpa::attn_fwd_kernel<BF16, MODE, HD, HDV, BIAS>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<BF16, MODE, HD, HDV>::SMEM_BYTES) != cudaSuccess)
+    return SDPA_ERR_CUDA;
+  st->attr_set[idx] = true;
+  return SDPA_OK;
+}
+
+template <bool BF16, int MODE, int HD, int HDV>
+void fill_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, long long ctas,
+                 cudaStream_t stream) {
+  constexpr bool kCluster = MODE != gbsdpa::kSingle;
+  *cfg = {};
+  cfg->gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+  cfg->blockDim = dim3(Cfg<BF16, MODE, HD, HDV>::NTHREADS, 1, 1);
+  cfg->dynamicSmemBytes = Cfg<BF16, MODE, HD, HDV>::SMEM_BYTES;
+  cfg->stream = stream;
+  cfg->attrs = attr;
+  cfg->numAttrs = 0;
+  if (kCluster) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg->numAttrs = 1;
+  }
+}
+
+template <bool BF16, int MODE, int HD, int HDV, bool BIAS>
+int launch_attn(const AttnParams& p, long long items, cudaStream_t stream, DeviceState* st) {
+  int rc = ensure_attr<BF16, MODE, HD, HDV, BIAS>(st);
+  if (rc) return rc;
+  constexpr bool kCluster = MODE != gbsdpa::kSingle;
+  const long long ctas = items * (kCluster ? 2 : 1);
+  if (ctas <= 0 || ctas > 0x7fffffffll) return SDPA_ERR_INVALID_ARG;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  // A persistent grid waits on itself (prefix units on suffix units).  It is
+  // sized to the occupancy limit, so on an otherwise idle GPU all of it is
+  // resident; the kernel starts the never-waiting units first, and a wait that
+  // still runs out reports a device timeout instead of hanging.
+  fill_launch<BF16, MODE, HD, HDV>(&cfg, attr, ctas, stream);
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, gbsdpa::attn_fwd_kernel<BF16, MODE, HD, HDV, BIAS>, p);
+  return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+// How many persistent units (CTAs, or CTA pairs for the 2-SM variant) can be
+// resident at once on this device; 0 if the variant cannot run persistently.
+template <bool BF16, int MODE, int HD, int HDV, bool BIAS>
+int resident_units(DeviceState* st) {
+  constexpr int idx = variant_index<BF16, MODE, HD, HDV, BIAS>();
+  if (st->sk_units[idx]) return st->sk_units[idx];
+  if (ensure_attr<BF16, MODE, HD, HDV, BIAS>(st)) return 0;
+  auto kern = gbsdpa::attn_fwd_kernel<BF16, MODE, HD, HDV, BIAS>;
+  int units = 0;
+  if (MODE == gbsdpa::kSingle) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern,
+                                                      Cfg<BF16, MODE, HD, HDV>::NTHREADS,
+                                                      Cfg<BF16, MODE, HD, HDV>::SMEM_BYTES) !=
+        cudaSuccess)
+      return 0;
+    units = per_sm * st->sms;
+  } else {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    fill_launch<BF16, MODE, HD, HDV>(&cfg, attr, 2 * (st->sms / 2), nullptr);
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) return 0;
+    units = clusters;
+  }
+  st->sk_units[idx] = std::max(0, units);
+  return st->sk_units[idx];
+}
+
+// Run-time choice of the instantiation: variant `mode`, Q/K head dim D, V head
+// dim Dv (the pairs the host validation admits).
+template <bool BF16, bool BIAS>
+int launch_variant(int mode, int D, int Dv, const AttnParams& p, long long items,
+                   cudaStream_t stream, DeviceState* st) {
+  using gbsdpa::kDuo;
+  using gbsdpa::kPair;
+  using gbsdpa::kSingle;
+  switch (mode) {
+    case kPair: return launch_attn<BF16, kPair, 256, 256, BIAS>(p, items, stream, st);
+    case kDuo:
+      return D == 128 ? launch_attn<BF16, kDuo, 128, 128, BIAS>(p, items, stream, st)
+                      : launch_attn<BF16, kDuo, 256, 256, BIAS>(p, items, stream, st);
+    default:
+      return D != Dv    ? launch_attn<BF16, kSingle, 192, 256, BIAS>(p, items, stream, st)
+             : D == 128 ? launch_attn<BF16, kSingle, 128, 128, BIAS>(p, items, stream, st)
+             : D == 192 ? launch_attn<BF16, kSingle, 192, 192, BIAS>(p, items, stream, st)
+                        : launch_attn<BF16, kSingle, 256, 256, BIAS>(p, items, stream, st);
+  }
+}
+
+// Resident persistent units of the instantiation a prefill with these head dims
+// runs (0: not persistent: the head-dim-split pair, or a failed query).
+template <bool BF16, bool BIAS>
+int resident_variant(int mode, int D, int Dv, DeviceState* st) {
+  using gbsdpa::kDuo;
+  using gbsdpa::kSingle;
+  if (mode == kSingle)
+    return D != Dv    ? resident_units<BF16, kSingle, 192, 256, BIAS>(st)
+           : D == 128 ? resident_units<BF16, kSingle, 128, 128, BIAS>(st)
+           : D == 192 ? resident_units<BF16, kSingle, 192, 192, BIAS>(st)
+                      : resident_units<BF16, kSingle, 256, 256, BIAS>(st);
+  if (mode == kDuo)
+    return D == 128 ? resident_units<BF16, kDuo, 128, 128, BIAS>(st)
+                    : resident_units<BF16, kDuo, 256, 256, BIAS>(st);
+  return 0;
+}
+
+// The kernels with a bias, instantiated in sdpa_bias.cu.
+int launch_bias_variant(bool bf16, int mode, int D, int Dv, const AttnParams& p, long long items,
+                        cudaStream_t stream, DeviceState* st);
+int resident_bias_variant(bool bf16, int mode, int D, int Dv, DeviceState* st);
+
+}  // namespace gbsdpa_host

@@ -272,6 +272,38 @@ def suite(gb, device, flush, stream, hbm, bf16_peak):
                                        "bytes": decode_bytes(w)}
             del q, k, v, out, ws
             torch.cuda.empty_cache()
+    # additive bias (mask array): one [Lq, Lk] mask shared by all heads in prefill,
+    # one row per (head, query) in decode; entries N(0, 1) with a quarter -inf
+    g = torch.Generator(device=device).manual_seed(5)
+    for w, decode in ((wl.LONGKV, False), (wl.DECODE_WORKLOADS[0].with_(Lq=1), True)):
+        q, k, v = wl.make_qkv(w, device=device)
+        out = torch.empty_like(q)
+        shape = (1, w.Hq, w.Lq, w.Lk) if decode else (1, 1, w.Lq, w.Lk)
+        bias = torch.randn(shape, generator=g, device=device)
+        bias = bias.masked_fill(torch.rand(shape, generator=g, device=device) < 0.25,
+                                float("-inf")).to(q.dtype)
+        if decode:
+            ws = torch.empty(gb.decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.Lq, w.D),
+                             dtype=torch.uint8, device=device)
+            fn = lambda: gb.sdpa_decode(q, k, v, out, scale=w.scale, causal=w.causal,
+                                        window=w.window, workspace=ws, bias=bias)
+            ms = statistics.median(time_calls(fn, 20, 5, flush, stream))
+            byts = decode_bytes(w) + w.B * w.Hq * w.Lq * min(w.Lk, w.window or w.Lk) * 2
+            res[f"{w.name}_Lq1_bias"] = {"us": round(ms * 1e3, 2),
+                                         "GBps": round(byts / ms / 1e6, 1), "bytes": byts}
+        else:
+            ws = torch.empty(max(1, gb.prefill_workspace_bytes(
+                w.B, w.Hq, w.Hkv, w.Lq, w.Lk, w.D, w.causal, w.window)),
+                dtype=torch.uint8, device=device)
+            fn = lambda: gb.sdpa_prefill(q, k, v, out, scale=w.scale, causal=w.causal,
+                                         window=w.window, workspace=ws, bias=bias)
+            ms = statistics.median(time_calls(fn, 10, 3, flush, stream))
+            tf = prefill_flops(w) / ms / 1e9
+            res[f"{w.name}_bias"] = {"ms": round(ms, 4), "tflops": round(tf, 1),
+                                     "frac_of_bf16_peak": round(tf / bf16_peak, 4),
+                                     "bias_bytes": bias.numel() * 2}
+        del q, k, v, out, ws, bias
+        torch.cuda.empty_cache()
     # transient device memory against kL at the long-KV GQA head geometry
     trans = {}
     for qL, kL in ((1024, 32768), (2048, 65536), (2048, 131072)):

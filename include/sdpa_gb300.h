@@ -143,8 +143,8 @@ int sdpa_decode(const void* q, const void* k, const void* v, void* out, int B, i
 size_t sdpa_decode_workspace_bytes(int B, int Hq, int Hkv, int Lq, int D);
 
 /*
- * Extended prefill / decode: a V head dim that differs from Q/K's, and K/V read
- * from a caller's cache instead of packed tensors.
+ * Extended prefill / decode: a V head dim that differs from Q/K's, K/V read
+ * from a caller's cache instead of packed tensors, and an additive bias.
  *
  * Head dims.  q and k have Dqk columns, v and out have Dv.  Supported: Dqk ==
  * Dv in {128, 192, 256, 512}, and Dqk = 192 with Dv = 256, the Q=192/K=192/
@@ -173,19 +173,39 @@ size_t sdpa_decode_workspace_bytes(int B, int Hq, int Hkv, int Lq, int D);
  * the same call on packed copies of the keys, so decode row invariance holds
  * over the trimmed prefix of the same cache.
  *
+ * Additive bias (a mask array).  "fix: gemma-4 long-prompt prefill OOMs on
+ * CUDA" (mlxcel issue #672, sections "Root cause" and "Suggested fix
+ * direction") describes models that hand attention a dense additive mask (0 for
+ * a visible key, -inf for a hidden one) and cuDNN's flash path that takes such
+ * a mask as a bias.  With bias != NULL the score of query row i and key j is
+ *     scale * q_i . k_j + bias[b * bias_stride_b + h * bias_stride_h
+ *                              + i * bias_stride_q + j]
+ * for query head h, on top of the causal / window flags (keys they hide stay
+ * hidden).  The bias is in q's dtype, device memory, owned by the caller and
+ * only read; strides are in elements and >= 0, and a stride of 0 broadcasts
+ * (a [1, 1, Lq, Lk] mask shared by all heads has bias_stride_b =
+ * bias_stride_h = 0, bias_stride_q = Lk).  Key j is the logical key position
+ * 0..Lk-1, also for a ring cache.  Entries may be finite or -inf (not +inf or
+ * NaN); a row whose keys are all hidden outputs zeros.  Base and strides that
+ * are multiples of 16 bytes are read in vectors, others element by element.
+ * Negative or huge strides: SDPA_ERR_INVALID_ARG; an odd address:
+ * SDPA_ERR_ALIGNMENT.  bias = NULL: no bias (strides ignored).
+ *
  * Everything else is as for sdpa_prefill / sdpa_decode.  Unsupported head dims
  * return SDPA_ERR_UNSUPPORTED and layout errors SDPA_ERR_INVALID_ARG before
  * anything is queued.
  */
 int sdpa_prefill_ex(const void* q, const void* k, const void* v, void* out, int B, int Hq,
                     int Hkv, int Lq, int Lk, int Dqk, int Dv, float scale, int causal, int window,
-                    int dtype, int kv_capacity, int kv_ring, void* workspace,
-                    size_t workspace_bytes, sdpa_stream_t stream);
+                    int dtype, int kv_capacity, int kv_ring, const void* bias,
+                    long long bias_stride_b, long long bias_stride_h, long long bias_stride_q,
+                    void* workspace, size_t workspace_bytes, sdpa_stream_t stream);
 
 int sdpa_decode_ex(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
                    int Lq, int Lk, int Dqk, int Dv, float scale, int causal, int window,
-                   int dtype, int kv_capacity, int kv_ring, void* workspace,
-                   size_t workspace_bytes, sdpa_stream_t stream);
+                   int dtype, int kv_capacity, int kv_ring, const void* bias,
+                   long long bias_stride_b, long long bias_stride_h, long long bias_stride_q,
+                   void* workspace, size_t workspace_bytes, sdpa_stream_t stream);
 
 /* Synchronises `stream`, returns SDPA_OK or SDPA_ERR_DEVICE_TIMEOUT for the
  * current device and clears the status word.  *detail (if not NULL) receives

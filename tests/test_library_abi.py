@@ -91,9 +91,10 @@ def test_launch_query_rejects_bad_arguments_on_the_host(lib):
     assert lib.sdpa_prefill_launches(1, 2, 1, 9, 8, 256, 1, 0, 0) == -1   # causal Lq > Lk
 
 
-def call_ex(lib, fn, cap, ring, Lq=4, Lk=3000, window=1024, causal=1, Dqk=256, Dv=256):
+def call_ex(lib, fn, cap, ring, Lq=4, Lk=3000, window=1024, causal=1, Dqk=256, Dv=256,
+            bias=None, sb=0, sh=0, sq=0):
     return getattr(lib, fn)(FAKE, FAKE, FAKE, FAKE, 1, 2, 1, Lq, Lk, Dqk, Dv, 0.0625, causal,
-                            window, 0, cap, ring, FAKE, 1 << 20, None)
+                            window, 0, cap, ring, bias, sb, sh, sq, FAKE, 1 << 20, None)
 
 
 @pytest.mark.parametrize("fn", ["sdpa_prefill_ex", "sdpa_decode_ex"])
@@ -115,3 +116,12 @@ def test_unequal_head_dims_are_checked_on_the_host(lib, fn):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError):
         gb.load_library(str(tmp_path / "nope.so"))
+
+
+@pytest.mark.parametrize("fn", ["sdpa_prefill_ex", "sdpa_decode_ex"])
+def test_bias_arguments_are_checked_on_the_host(lib, fn):
+    ok = dict(cap=3000, ring=0)
+    assert call_ex(lib, fn, bias=FAKE, sb=-8, **ok) == -1
+    assert call_ex(lib, fn, bias=FAKE, sh=-1, **ok) == -1
+    assert call_ex(lib, fn, bias=FAKE, sq=1 << 60, **ok) == -1
+    assert call_ex(lib, fn, bias=ctypes.c_void_p(0x10001), sq=3000, **ok) == -6   # odd address
