@@ -335,6 +335,9 @@ def profile_run(args):
     from attention_sm_flash_attn_gb300 import build as gbbuild
     gbbuild.build()
     name, lq = args.profile, None
+    with_bias = name.endswith("_bias")
+    if with_bias:
+        name = name[:-len("_bias")]
     if "_Lq" in name:
         name, lq = name.rsplit("_Lq", 1)
     table = {w.name: w for w in wl.PREFILL_WORKLOADS + wl.DECODE_WORKLOADS}
@@ -343,21 +346,31 @@ def profile_run(args):
         w = w.with_(Lq=int(lq))
     q, k, v = wl.make_qkv(w, device="cuda")
     out = torch.empty_like(q)
+    bias = None
+    if with_bias:
+        # the suite's bias: one [Lq, Lk] mask for all heads in prefill, one row
+        # per (head, query) in decode; N(0, 1) entries, a quarter of them -inf
+        g = torch.Generator(device="cuda").manual_seed(5)
+        shape = (1, w.Hq, w.Lq, w.Lk) if w.kind == "decode" else (1, 1, w.Lq, w.Lk)
+        bias = torch.randn(shape, generator=g, device="cuda")
+        bias = bias.masked_fill(torch.rand(shape, generator=g, device="cuda") < 0.25,
+                                float("-inf")).to(q.dtype)
     if w.kind == "decode":
         ws = torch.empty(gb.decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.Lq, w.D),
                          dtype=torch.uint8, device="cuda")
         fn = lambda: gb.sdpa_decode(q, k, v, out, scale=w.scale, causal=w.causal,
-                                    window=w.window, workspace=ws)
+                                    window=w.window, workspace=ws, bias=bias)
     else:
         nb = gb.prefill_workspace_bytes(w.B, w.Hq, w.Hkv, w.Lq, w.Lk, w.D, w.causal, w.window)
         ws = torch.empty(max(1, nb), dtype=torch.uint8, device="cuda")
         fn = lambda: gb.sdpa_prefill(q, k, v, out, scale=w.scale, causal=w.causal,
-                                     window=w.window, workspace=ws)
+                                     window=w.window, workspace=ws, bias=bias)
     for _ in range(args.warmup + args.steps):
         fn()
     torch.cuda.synchronize()
     st = gb.device_status()
-    print(json.dumps({"profile": w.name, "Lq": w.Lq, "calls": args.warmup + args.steps,
+    print(json.dumps({"profile": w.name, "Lq": w.Lq, "bias": with_bias,
+                      "calls": args.warmup + args.steps,
                       "device_status": st[0]}))
     return 0 if st[0] == 0 else 1
 
@@ -479,7 +492,8 @@ def main():
                     help="seconds of oracle work per timed step of the reference arm")
     ap.add_argument("--profile", default=None,
                     help="run one named workload --steps times (for ncu) and exit; decode "
-                         "workloads take a _LqN suffix")
+                         "workloads take a _LqN suffix, and a _bias suffix adds the suite's "
+                         "additive bias")
     ap.add_argument("--routing", action="store_true",
                     help="fused vs unfused (cuBLAS matmul + softmax + matmul) prefill time over "
                          "kL, one JSON line, and exit")
