@@ -10,21 +10,27 @@
 //   (!causal || j <= p) && (window == 0 || p - j < window):
 //     out[h, i] = sum_j softmax_j(scale * q_i . k_j) v_j
 //
-// One CTA owns 128 query rows (one tcgen05 M=128 tile) and walks a list of
-// key tiles.  Warp roles:
-//   warps 0-3  softmax + epilogue: one thread per row / TMEM lane
-//   warp  4    TMA producer: Q once, then K and V sub-tiles into a ring
-//   warp  5    TMEM allocator and tcgen05.mma issuer
+// One CTA owns 128 query rows (one tcgen05 M=128 tile; 256 rows per CTA pair
+// in the 2-SM variant) and walks a list of key tiles.  Warp roles (384
+// threads):
+//   warps 0-7  softmax + epilogue: two threads per row / TMEM lane, warps q
+//              and q+4 owning the two halves of the key (and O) columns
+//   warp  8    TMA producer: Q, then K and V sub-tiles into a ring
+//   warp  9    TMEM allocator and tcgen05.mma issuer
+//   warps 10-11 idle (they complete the third warpgroup of the register split)
 // Per key tile j:  S_j = Q K_j^T (tcgen05, fp32 in TMEM, double buffered)
 //                  softmax warps: tcgen05.ld S_j, mask, online max/sum (log2
 //                  domain, lazy rescale), P_j -> shared memory (fp16/bf16)
 //                  O += P_j V_j  (tcgen05, fp32 in TMEM)
-// Whole key tiles outside the causal/window band are never visited.
+// Whole key tiles outside the causal/window band are never visited.  With
+// BIAS, an additive bias (a mask array) is added to the scaled scores.
 //
 // Modes:
-//  * prefill: 128 consecutive query rows of one head; either the whole visible
-//    key range (final output) or one contiguous share of it (fp32 partials
-//    merged by the combine kernel);
+//  * prefill: 128 (or 256) consecutive query rows of one head; either the
+//    whole visible key range (final output), one contiguous share of it (fp32
+//    partials merged by the combine kernel), or, in the persistent schedule,
+//    a sequence of pieces of several query tiles with suffix pieces merged by
+//    the unit that owns the tile's prefix;
 //  * decode (Lq <= 8): the 128 rows are 16 query heads x 8 slots of one kv
 //    head; query row i goes to slot (p_i mod 8), so the same row always lands
 //    on the same TMEM lane whatever Lq is.  Key tiles are dealt round-robin

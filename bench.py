@@ -86,15 +86,42 @@ def peaks():
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "attn_fwd_duo_longkv_gqa_prefill_hd256.txt")
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without // and /* */ comments, trailing blanks and empty
+    lines (string and character literals are kept as they are)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            while i < n and src[i] != "\n":
+                i += 1
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = (line.rstrip() for line in "".join(out).split("\n"))
+    return "\n".join(line for line in lines if line)
+
+
 def kernel_sources_digest() -> str:
-    """sha256 over the CUDA sources and the public header, in name order."""
+    """sha256 over the code (comments stripped) of the CUDA sources and the public
+    header, in name order: a comment edit leaves the digest, and so the profiled
+    traffic, in force; any code change retires it."""
     files = sorted(glob.glob(os.path.join(ROOT, "attention_sm_flash_attn_gb300", "csrc", "*.cu*"))
                    + glob.glob(os.path.join(ROOT, "include", "*.h")))
     h = hashlib.sha256()
     for f in files:
         h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(strip_comments(fh.read()).encode())
     return h.hexdigest()
 
 

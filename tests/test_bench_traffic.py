@@ -13,3 +13,13 @@ def test_traffic_is_reported_only_for_matching_sources(tmp_path, monkeypatch):
     assert bench.profiled_traffic() is None
     monkeypatch.setattr(bench, "TRAFFIC_SUMMARY", str(tmp_path / "missing.txt"))
     assert bench.profiled_traffic() is None
+
+
+def test_digest_sees_code_not_comments():
+    a = "int f(int x) {  // doubles\n  return 2 * x; /* no overflow here */\n}\n"
+    b = "/* header */\nint f(int x) {\n\n  return 2 * x;\n}\n"
+    c = "int f(int x) {\n  return 3 * x;\n}\n"
+    assert bench.strip_comments(a) == bench.strip_comments(b)
+    assert bench.strip_comments(a) != bench.strip_comments(c)
+    s = 'asm("mov.u32 %0, 1; // kept");\n'
+    assert bench.strip_comments(s) == s.strip()
