@@ -155,9 +155,8 @@ struct Cfg {
   static constexpr int V_SLOT_BYTES = VBOX * V_LBO;
   static constexpr int Q_OFF = 0;
   static constexpr int RING_OFF = 65536;
-  static constexpr int P_OFF = RING_OFF + NSLOT * SLOT;
-  static constexpr int P_BYTES = BM * BN * 2;
-  static constexpr int X_OFF = P_OFF + P_BYTES;      // peer's partial scores (received)
+  // (P lives in tensor memory, over the S buffer it came from.)
+  static constexpr int X_OFF = RING_OFF + NSLOT * SLOT;  // peer's partial scores (received)
   static constexpr int X_BYTES = PAIR ? BM * BN * 4 : 0;
   static constexpr int XS_OFF = X_OFF + X_BYTES;     // own partial scores (staged to send)
   static constexpr int BAR_OFF = XS_OFF + X_BYTES;
@@ -529,7 +528,6 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
   const uint32_t sbase = ptx::smem_u32(smem);
   const uint32_t sQ = sbase + C::Q_OFF;
   const uint32_t sRing = sbase + C::RING_OFF;
-  const uint32_t sP = sbase + C::P_OFF;
   const uint32_t sX = sbase + C::X_OFF;
   const uint32_t sBar = sbase + C::BAR_OFF;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::BAR_OFF + 240);
@@ -743,8 +741,9 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
         ++n;
       };
       auto do_s = [&](int gt) {
-        // S buffer gt % 2 last held S_{gt-2}; the softmax read it before it
-        // produced P_{gt-2}, and the P.V of tile gt - 2 has already waited for it.
+        // S buffer gt % 2 last held S_{gt-2} and then P_{gt-2}; the P.V of tile
+        // gt - 2 that reads P was issued before this product, and the tensor
+        // pipe runs one thread's MMAs in issue order.
         const uint32_t d_tmem = tmem + C::S_COL + (gt & 1) * BN;
         for (int ks = 0; ks < C::KSUB; ++ks) {
           uint32_t sk;
@@ -792,10 +791,13 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
 #pragma unroll
           for (int kk = 0; kk < C::VROWS / 16; ++kk) {
             const int key = vs * C::VROWS + kk * 16;
-            const uint64_t a =
-                ptx::sdesc_sw128(sP + (key / 64) * 16384 + (key % 64) * 2, 16, 1024);
+            // A = P_gt in tensor memory (keys key..key+15 at columns key / 2).
+            const uint32_t a = tmem + C::S_COL + (gt & 1) * BN + key / 2;
             const uint64_t b = ptx::sdesc_sw128(sv + kk * 2048, C::V_LBO, 1024);
-            mma(tmem, a, b, C::IDESC_PV, (j | vs | kk) != 0);
+            if constexpr (DUO)
+              ptx::mma_f16_ts_pair(tmem, a, b, C::IDESC_PV, (j | vs | kk) != 0);
+            else
+              ptx::mma_f16_ts(tmem, a, b, C::IDESC_PV, (j | vs | kk) != 0);
           }
           release();
           ++mma_issued;
@@ -1125,8 +1127,10 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
         }
         l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
 
-        // The P buffer and O are free once the previous P.V product of this
-        // piece has completed (the previous piece's epilogue waited for its own).
+        // O may be rescaled once the previous P.V product of this piece has
+        // completed (the previous piece's epilogue waited for its own).  The
+        // wait is taken on every tile so that this barrier's phases stay within
+        // one of the waiter's (a parity wait cannot tell phase k from k + 2).
         if (j > 0 && alive)
           alive = __all_sync(0xffffffffu, wait_bar(bar(kBarPvDone), (gt - 1) & 1, abort_flag,
                                                    p.status, kDevTimeoutPvDone));
@@ -1149,17 +1153,18 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
           }
           ptx::tmem_wait_st();
         }
-        // P row -> shared memory, K-major 128B-swizzled (64 keys per 128-byte row).
-#pragma unroll
-        for (int ch = 0; ch < HB / 8; ++ch) {
-          const int gc = half * (HB / 8) + ch;
-          const int blk = gc >> 3, cc = gc & 7;
-          const uint32_t addr = sP + blk * 16384 + t * 128 + ((cc ^ (t & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * ch]),
-                       "r"(pk[4 * ch + 1]), "r"(pk[4 * ch + 2]), "r"(pk[4 * ch + 3])
-                       : "memory");
+        // P row -> tensor memory, over the first BN/2 columns of the S buffer
+        // it came from (two 16-bit probabilities per column; this thread's keys
+        // at columns [half * HB/2, (half + 1) * HB/2)).  The other half of the
+        // row has read its S columns: both passed the row-max swap.
+        {
+          const uint32_t pcol = lane_base + C::S_COL + buf * BN + half * (HB / 2);
+          if constexpr (HB == 64)
+            ptx::tmem_st32(pcol, pk);
+          else
+            ptx::tmem_st16(pcol, pk);
+          ptx::tmem_wait_st();
         }
-        ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         warp_arrive(kBarPFull);
       }
