@@ -313,6 +313,20 @@ __device__ __forceinline__ void mma_f16_ts_pair(uint32_t d_tmem, uint32_t a_tmem
       : "memory");
 }
 
+// Copy a 128-row x 256-bit matrix from shared memory (described like an MMA
+// operand: `sdesc` with its swizzle) into tensor memory: row i to lane i,
+// columns [taddr, taddr + 8).  Ordered with this thread's other tcgen05
+// operations; tcgen05.commit tracks its completion.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// 2-SM form: each CTA of the pair copies from its own shared memory into its
+// own tensor memory at the same offsets.
+__device__ __forceinline__ void tmem_cp_128x256b_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // 2-SM commit: arrive once on the mbarrier at offset `bar` in every CTA of
 // `cta_mask` when all prior 2-SM MMAs of this thread have completed.
 __device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {

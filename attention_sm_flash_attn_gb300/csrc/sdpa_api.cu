@@ -186,7 +186,17 @@ int choose_mode(bool decode, int D, int window) {
 }
 
 
-int qtile_rows(int mode) { return mode == gbsdpa::kDuo ? 256 : 128; }
+// The instantiation a call of this shape launches: at head dim 256 with no
+// window and no bias the 2-SM variant keeps Q in tensor memory (measured
+// faster over long key ranges; a window's short pieces and a bias's loads do
+// better with the form that keeps P in tensor memory).
+int launch_mode(int mode, int D, int Dv, int window, bool bias) {
+  return (mode == gbsdpa::kDuo && D == 256 && Dv == 256 && window == 0 && !bias) ? gbsdpa::kDuoQ
+                                                                                 : mode;
+}
+
+bool two_sm(int mode) { return mode == gbsdpa::kDuo || mode == gbsdpa::kDuoQ; }
+int qtile_rows(int mode) { return two_sm(mode) ? 256 : 128; }
 int key_tile(int mode) { return mode == gbsdpa::kPair ? 64 : 128; }
 
 // Key tiles the longest query tile (of `rows` rows) visits.
@@ -340,8 +350,9 @@ template <bool BF16>
 long long persistent_units(DeviceState* st, int mode, int D, int B, int Hq, int Lq, int Lk,
                            int causal, int window, int Dv = 0, bool bias = false) {
   if (Dv <= 0) Dv = D;
-  const int units = bias ? gbsdpa_host::resident_bias_variant(BF16, mode, D, Dv, st)
-                         : gbsdpa_host::resident_variant<BF16, false>(mode, D, Dv, st);
+  const int lm = launch_mode(mode, D, Dv, causal ? window : 0, bias);
+  const int units = bias ? gbsdpa_host::resident_bias_variant(BF16, lm, D, Dv, st)
+                         : gbsdpa_host::resident_variant<BF16, false>(lm, D, Dv, st);
   if (units <= 0) return 0;
   const long long W =
       total_key_tiles(B, Hq, Lq, Lk, causal, window, key_tile(mode), qtile_rows(mode));
@@ -362,7 +373,7 @@ int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, i
   // K boxes: all keys of a tile (one CTA), or the CTA's 64 keys (pair kernels);
   // V boxes: 32 keys (one CTA, head-dim split) or 64 keys (2-SM MMA).
   const int k_rows = mode == gbsdpa::kSingle ? 128 : 64;
-  const int v_rows = mode == gbsdpa::kDuo ? 64 : 32;
+  const int v_rows = two_sm(mode) ? 64 : 32;
   int rc = SDPA_OK;
   if (!decode) rc = encode_map(&p.tm_q, q, D, Lq, static_cast<long long>(B) * Hq, 128, BF16);
   if (rc) return rc;
@@ -434,8 +445,9 @@ int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, i
     items = static_cast<long long>(B) * Hkv * n_splits * p.n_hb;
   else
     items = static_cast<long long>(B) * Hq * p.n_qtiles * n_splits;
-  rc = p.bias ? gbsdpa_host::launch_bias_variant(BF16, mode, D, Dv, p, items, stream, st)
-              : gbsdpa_host::launch_variant<BF16, false>(mode, D, Dv, p, items, stream, st);
+  const int lm = launch_mode(mode, D, Dv, window, p.bias != nullptr);
+  rc = p.bias ? gbsdpa_host::launch_bias_variant(BF16, lm, D, Dv, p, items, stream, st)
+              : gbsdpa_host::launch_variant<BF16, false>(lm, D, Dv, p, items, stream, st);
   if (rc) return rc;
   if (write_partial)
     rc = launch_combine(p.part_o, p.part_ml, out, R, Dv, n_splits, BF16, stream);

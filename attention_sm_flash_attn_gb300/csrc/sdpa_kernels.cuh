@@ -127,12 +127,14 @@ struct AttnParams {
 //   kDuo:    head_dim 256 prefill with 2-SM MMAs (cta_group::2): a 2-CTA
 //            cluster owns 256 query rows; each CTA loads half of every K and V
 //            tile, which halves the bytes each SM stages per FLOP.
-enum Mode : int { kSingle = 0, kPair = 1, kDuo = 2 };
+//   kDuoQ:   the 2-SM variant with Q in tensor memory (Q.K^T reads its A
+//            operand from TMEM), one S buffer and P in shared memory.
+enum Mode : int { kSingle = 0, kPair = 1, kDuo = 2, kDuoQ = 3 };
 
 template <bool BF16, int MODE, int HD = 256, int HDV = HD>
 struct Cfg {
   static constexpr bool PAIR = MODE == kPair;
-  static constexpr bool DUO = MODE == kDuo;
+  static constexpr bool DUO = MODE == kDuo || MODE == kDuoQ;
   static constexpr int BM = 128;                   // query rows per CTA
   static constexpr int DH = HD;                    // Q/K head-dim columns owned by one CTA
   static constexpr int DV = HDV;                   // V (and output) head-dim columns
@@ -155,8 +157,14 @@ struct Cfg {
   static constexpr int V_SLOT_BYTES = VBOX * V_LBO;
   static constexpr int Q_OFF = 0;
   static constexpr int RING_OFF = 65536;
-  // (P lives in tensor memory, over the S buffer it came from.)
-  static constexpr int X_OFF = RING_OFF + NSLOT * SLOT;  // peer's partial scores (received)
+  // Q in tensor memory (kDuoQ): Q.K^T reads its A operand from TMEM, which
+  // leaves room for one S buffer only, and P goes through shared memory.  The
+  // other variants keep Q in shared memory, two S buffers, and P in TMEM over
+  // the S buffer it came from.
+  static constexpr bool QTM = MODE == kDuoQ;
+  static constexpr int P_OFF = RING_OFF + NSLOT * SLOT;
+  static constexpr int P_BYTES = QTM ? BM * BN * 2 : 0;
+  static constexpr int X_OFF = P_OFF + P_BYTES;      // peer's partial scores (received)
   static constexpr int X_BYTES = PAIR ? BM * BN * 4 : 0;
   static constexpr int XS_OFF = X_OFF + X_BYTES;     // own partial scores (staged to send)
   static constexpr int BAR_OFF = XS_OFF + X_BYTES;
@@ -166,6 +174,8 @@ struct Cfg {
   static constexpr int ITER_OFF = RED_OFF + 2048;
   static constexpr int SMEM_BYTES = ITER_OFF + 768;
   static constexpr int S_COL = 256;  // TMEM: O in columns [0,256), S buffers after it
+  static constexpr int NSBUF = QTM ? 1 : 2;          // S buffers
+  static constexpr int Q_COL = S_COL + NSBUF * BN;   // Q (QTM): DH/2 columns
   // warps 0-7 softmax (warpgroups 0, 1), 8 producer, 9 MMA, 10-11 idle (warpgroup 2)
   static constexpr int NTHREADS = 384;
   // Registers a thread after the split; the sum stays within the launch
@@ -183,7 +193,7 @@ struct Cfg {
   // Arrivals completing P-full on the MMA CTA: one per softmax warp of each CTA
   // whose P rows the MMA reads.
   static constexpr int kPFullArrivals = DUO ? 16 : 8;
-  static_assert(S_COL + 2 * BN <= 512, "TMEM budget");
+  static_assert(S_COL + NSBUF * BN + (QTM ? DH / 2 : 0) <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(KSUB * KBOX * 64 == DH && VSUB * VROWS == BN, "tile decomposition");
   static_assert(VBOX * 64 == (DUO ? DV / 2 : DV) && V_SLOT_BYTES <= SLOT && K_SLOT_BYTES == SLOT,
@@ -205,8 +215,10 @@ enum {
   kBarXFull = 23,
   kBarXFree = 24,
   kBarDrain = 25,
-  kNumBars = 26,
+  kBarSFree = 26,    // Q in TMEM: the softmax has read the (single) S buffer
+  kNumBars = 27,
 };
+static_assert(kNumBars * 8 <= 240, "barriers end below the TMEM slot and abort flag");
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 
@@ -530,6 +542,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
   const uint32_t sRing = sbase + C::RING_OFF;
   const uint32_t sX = sbase + C::X_OFF;
   const uint32_t sBar = sbase + C::BAR_OFF;
+  const uint32_t sP = sbase + C::P_OFF;  // P (Q in TMEM only)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::BAR_OFF + 240);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 244);
   float* red = reinterpret_cast<float*>(smem + C::RED_OFF);
@@ -582,6 +595,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
     ptx::mbar_init(bar(kBarXFull), 1);  // local expect_tx arrive + the peer's bulk-copy bytes
     ptx::mbar_init(bar(kBarXFree), 8);  // one arrive per softmax warp of the peer
     ptx::mbar_init(bar(kBarDrain), 1);
+    ptx::mbar_init(bar(kBarSFree), C::kPFullArrivals);
     *abort_flag = 0;
     ptx::fence_mbarrier_init();
   }
@@ -741,10 +755,21 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
         ++n;
       };
       auto do_s = [&](int gt) {
-        // S buffer gt % 2 last held S_{gt-2} and then P_{gt-2}; the P.V of tile
-        // gt - 2 that reads P was issued before this product, and the tensor
-        // pipe runs one thread's MMAs in issue order.
-        const uint32_t d_tmem = tmem + C::S_COL + (gt & 1) * BN;
+        // Q in TMEM: the single S buffer is free once the softmax has read
+        // S_{gt-1}.  Otherwise S buffer gt % 2 last held S_{gt-2} and then
+        // P_{gt-2}; the P.V of tile gt - 2 that reads P was issued before this
+        // product, and the tensor pipe runs one thread's MMAs in issue order.
+        if constexpr (C::QTM) {
+          if (gt > 0) {
+            if (!wait_bar<DUO>(bar(kBarSFree), (gt - 1) & 1, abort_flag, p.status,
+                               kDevTimeoutSEmpty)) {
+              ok = false;
+              return;
+            }
+            ptx::tc_fence_after();
+          }
+        }
+        const uint32_t d_tmem = tmem + C::S_COL + (C::QTM ? 0 : (gt & 1) * BN);
         for (int ks = 0; ks < C::KSUB; ++ks) {
           uint32_t sk;
           if (!consume(sk)) {
@@ -756,16 +781,26 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
             const int dc = ks * C::KBOX + e;  // 64-column chunk of the head dim
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t a = ptx::sdesc_sw128(sQ + dc * 16384 + kk * 32, 16, 1024);
               const uint64_t b =
                   ptx::sdesc_sw128(sk + e * (C::KROWS * 128) + kk * 32, 16, 1024);
-              mma(d_tmem, a, b, C::IDESC_QK, (dc | kk) != 0);
+              if constexpr (C::QTM) {
+                // A = Q from tensor memory: head-dim columns [16 (4 dc + kk), +16)
+                // at TMEM columns Q_COL + 8 (4 dc + kk).
+                const uint32_t a = tmem + C::Q_COL + static_cast<uint32_t>((dc * 4 + kk) * 8);
+                if constexpr (DUO)
+                  ptx::mma_f16_ts_pair(d_tmem, a, b, C::IDESC_QK, (dc | kk) != 0);
+                else
+                  ptx::mma_f16_ts(d_tmem, a, b, C::IDESC_QK, (dc | kk) != 0);
+              } else {
+                const uint64_t a = ptx::sdesc_sw128(sQ + dc * 16384 + kk * 32, 16, 1024);
+                mma(d_tmem, a, b, C::IDESC_QK, (dc | kk) != 0);
+              }
             }
           }
           release();
           ++mma_issued;
         }
-        commit(kBarSFull + (gt & 1));
+        commit(kBarSFull + (C::QTM ? 0 : (gt & 1)));
       };
       auto do_pv = [&](int gt, int j) {  // j: tile index within the piece
         if (!wait_bar<DUO>(bar(kBarPFull), gt & 1, abort_flag, p.status, kDevTimeoutPFull)) {
@@ -791,13 +826,20 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
 #pragma unroll
           for (int kk = 0; kk < C::VROWS / 16; ++kk) {
             const int key = vs * C::VROWS + kk * 16;
-            // A = P_gt in tensor memory (keys key..key+15 at columns key / 2).
-            const uint32_t a = tmem + C::S_COL + (gt & 1) * BN + key / 2;
             const uint64_t b = ptx::sdesc_sw128(sv + kk * 2048, C::V_LBO, 1024);
-            if constexpr (DUO)
-              ptx::mma_f16_ts_pair(tmem, a, b, C::IDESC_PV, (j | vs | kk) != 0);
-            else
-              ptx::mma_f16_ts(tmem, a, b, C::IDESC_PV, (j | vs | kk) != 0);
+            if constexpr (C::QTM) {
+              // A = P_gt in shared memory (K-major, 128B-swizzled, 64 keys a row).
+              const uint64_t a =
+                  ptx::sdesc_sw128(sP + (key / 64) * 16384 + (key % 64) * 2, 16, 1024);
+              mma(tmem, a, b, C::IDESC_PV, (j | vs | kk) != 0);
+            } else {
+              // A = P_gt in tensor memory (keys key..key+15 at columns key / 2).
+              const uint32_t a = tmem + C::S_COL + (gt & 1) * BN + key / 2;
+              if constexpr (DUO)
+                ptx::mma_f16_ts_pair(tmem, a, b, C::IDESC_PV, (j | vs | kk) != 0);
+              else
+                ptx::mma_f16_ts(tmem, a, b, C::IDESC_PV, (j | vs | kk) != 0);
+            }
           }
           release();
           ++mma_issued;
@@ -815,11 +857,27 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
           break;
         }
         ptx::tc_fence_after();
+        if constexpr (C::QTM) {
+          // Q to tensor memory, 16 head-dim columns per copy; the previous
+          // piece's last Q.K^T, issued before, has read the old Q.  The query
+          // buffer in shared memory is free once these copies have completed.
+          for (int dc = 0; dc < C::DH / 64; ++dc)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t dst = tmem + C::Q_COL + static_cast<uint32_t>((dc * 4 + kk) * 8);
+              const uint64_t src = ptx::sdesc_sw128(sQ + dc * 16384 + kk * 32, 16, 1024);
+              if constexpr (DUO)
+                ptx::tmem_cp_128x256b_pair(dst, src);
+              else
+                ptx::tmem_cp_128x256b(dst, src);
+            }
+          commit(kBarQFree);
+        }
         do_s(g0);
-        if (ok && count == 1) commit(kBarQFree);
+        if (!C::QTM && ok && count == 1) commit(kBarQFree);
         for (int j = 1; j < count && ok; ++j) {
           do_s(g0 + j);
-          if (ok && j == count - 1) commit(kBarQFree);
+          if (!C::QTM && ok && j == count - 1) commit(kBarQFree);
           if (ok) do_pv(g0 + j - 1, j - 1);
         }
         if (ok) do_pv(g0 + count - 1, count - 1);
@@ -957,7 +1015,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
         const int gt = g0 + j;
         const int tile = w.t_begin + j * w.t_step;
         const int kb = tile * BN + half * HB;  // first key of this thread's columns
-        const int buf = gt & 1;
+        const int buf = C::QTM ? 0 : (gt & 1);  // S buffer of this tile
         float s[HB];
 #pragma unroll
         for (int e = 0; e < HB; ++e) s[e] = -INFINITY;
@@ -973,8 +1031,9 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
           }
         }
         if (alive)
-          alive = __all_sync(0xffffffffu, wait_bar(bar(kBarSFull + buf), (gt >> 1) & 1,
-                                                   abort_flag, p.status, kDevTimeoutSFull));
+          alive = __all_sync(0xffffffffu,
+                             wait_bar(bar(kBarSFull + buf), C::QTM ? (gt & 1) : ((gt >> 1) & 1),
+                                      abort_flag, p.status, kDevTimeoutSFull));
         if (BIAS && !PAIR && alive) {
           // Scores straight to the log2 domain, c * s + log2(e) * bias, one
           // 32-column chunk at a time (a masked key becomes -inf below).
@@ -1004,6 +1063,14 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
             ptx::reg_fence(r[cch]);
 #pragma unroll
             for (int e = 0; e < 32; ++e) s[cch * 32 + e] = __uint_as_float(r[cch][e]);
+          }
+        }
+        if constexpr (C::QTM) {
+          // Single S buffer: the next Q.K^T may overwrite it once every softmax
+          // warp has read its lanes (the loads above have completed).
+          if (alive) {
+            ptx::tc_fence_before();
+            warp_arrive(kBarSFree);
           }
         }
 
@@ -1153,11 +1220,23 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
           }
           ptx::tmem_wait_st();
         }
-        // P row -> tensor memory, over the first BN/2 columns of the S buffer
-        // it came from (two 16-bit probabilities per column; this thread's keys
-        // at columns [half * HB/2, (half + 1) * HB/2)).  The other half of the
-        // row has read its S columns: both passed the row-max swap.
-        {
+        if constexpr (C::QTM) {
+          // P row -> shared memory, K-major 128B-swizzled (64 keys per 128-byte row).
+#pragma unroll
+          for (int ch = 0; ch < HB / 8; ++ch) {
+            const int gc = half * (HB / 8) + ch;
+            const int blk = gc >> 3, cc = gc & 7;
+            const uint32_t addr = sP + blk * 16384 + t * 128 + ((cc ^ (t & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * ch]),
+                         "r"(pk[4 * ch + 1]), "r"(pk[4 * ch + 2]), "r"(pk[4 * ch + 3])
+                         : "memory");
+          }
+          ptx::fence_proxy_async_smem();
+        } else {
+          // P row -> tensor memory, over the first BN/2 columns of the S buffer
+          // it came from (two 16-bit probabilities per column; this thread's
+          // keys at columns [half * HB/2, (half + 1) * HB/2)).  The other half of
+          // the row has read its S columns: both passed the row-max swap.
           const uint32_t pcol = lane_base + C::S_COL + buf * BN + half * (HB / 2);
           if constexpr (HB == 64)
             ptx::tmem_st32(pcol, pk);

@@ -18,7 +18,7 @@ using gbsdpa::AttnParams;
 using gbsdpa::Cfg;
 
 // Slot of a kernel instantiation in the per-device tables: bias x dtype x
-// variant x per-CTA head dims (Q/K, V): (256, 256), (128, 128), (192, 192),
+// variant (4) x per-CTA head dims (Q/K, V): (256, 256), (128, 128), (192, 192),
 // (192, 256).
 template <bool BF16, int MODE, int HD, int HDV, bool BIAS>
 constexpr int variant_index() {
@@ -38,7 +38,7 @@ struct DeviceState {
 
 static_assert(variant_index<false, gbsdpa::kSingle, 192, 256, false>() !=
                       variant_index<false, gbsdpa::kSingle, 192, 192, false>() &&
-                  variant_index<true, gbsdpa::kDuo, 256, 256, true>() < kNumVariants,
+                  variant_index<true, gbsdpa::kDuoQ, 192, 256, true>() < kNumVariants,
               "distinct slots within the tables");
 
 template <bool BF16, int MODE, int HD, int HDV, bool BIAS>
@@ -127,10 +127,16 @@ template <bool BF16, bool BIAS>
 int launch_variant(int mode, int D, int Dv, const AttnParams& p, long long items,
                    cudaStream_t stream, DeviceState* st) {
   using gbsdpa::kDuo;
+  using gbsdpa::kDuoQ;
   using gbsdpa::kPair;
   using gbsdpa::kSingle;
   switch (mode) {
     case kPair: return launch_attn<BF16, kPair, 256, 256, BIAS>(p, items, stream, st);
+    case kDuoQ:
+      if constexpr (!BIAS)
+        return launch_attn<BF16, kDuoQ, 256, 256, false>(p, items, stream, st);
+      else
+        return SDPA_ERR_INVALID_ARG;  // never chosen with a bias
     case kDuo:
       return D == 128 ? launch_attn<BF16, kDuo, 128, 128, BIAS>(p, items, stream, st)
                       : launch_attn<BF16, kDuo, 256, 256, BIAS>(p, items, stream, st);
@@ -147,7 +153,14 @@ int launch_variant(int mode, int D, int Dv, const AttnParams& p, long long items
 template <bool BF16, bool BIAS>
 int resident_variant(int mode, int D, int Dv, DeviceState* st) {
   using gbsdpa::kDuo;
+  using gbsdpa::kDuoQ;
   using gbsdpa::kSingle;
+  if (mode == kDuoQ) {
+    if constexpr (!BIAS)
+      return resident_units<BF16, kDuoQ, 256, 256, false>(st);
+    else
+      return 0;
+  }
   if (mode == kSingle)
     return D != Dv    ? resident_units<BF16, kSingle, 192, 256, BIAS>(st)
            : D == 128 ? resident_units<BF16, kSingle, 128, 128, BIAS>(st)
