@@ -47,6 +47,9 @@ PREFILL_CASES = [
     (1, 4, 2, 150, 300, 512, True, 50),
     (1, 2, 2, 70, 129, 512, False, 0),
     (1, 2, 1, 129, 4100, 256, True, 0),     # long keys: split-KV prefill + combine
+    (1, 2, 1, 300, 100, 256, False, 0),     # non-causal, more queries than keys, keys < 1 tile
+    (1, 2, 2, 513, 65, 256, False, 0),      # query rows spill into a third 256-row tile
+    (3, 4, 4, 257, 1000, 256, True, 0),     # batch 3, one row past a 256-row tile
     (1, 2, 1, 256, 3000, 512, True, 0),     # long keys at head_dim 512
     # head_dim 192 (one-CTA variant) and 128 (2-SM variant, one CTA for short windows)
     (1, 2, 1, 128, 128, 192, True, 0),
@@ -177,3 +180,17 @@ def test_decode_agrees_with_prefill_within_tolerance():
     a = gb.sdpa_decode(qd, kd, vd, causal=True, window=1024)
     b = gb.sdpa_prefill(qd, kd, vd, causal=True, window=1024)
     assert float((a.float() - b.float()).abs().max()) < 4e-3
+
+
+@pytest.mark.parametrize("D", [128, 256, 512])
+def test_large_scale_exercises_the_rescale(D):
+    """scale = 1 on unit-variance inputs: row maxima jump by far more than the
+    lazy-rescale threshold from tile to tile, so O is rescaled in tensor
+    memory many times; the result still matches the oracle."""
+    Lq, Lk = 300, 2000
+    q, k, v = draw(1, 4, 2, Lq, Lk, D, torch.float16, seed=14 + D)
+    out = gb.sdpa_prefill(q.to(DEV), k.to(DEV), v.to(DEV), causal=True, scale=1.0)
+    torch.cuda.synchronize()
+    assert gb.device_status()[0] == 0
+    ref = oracle.sdpa(q, k, v, causal=True, scale=1.0)
+    assert max_err(out, ref) < 4e-3
