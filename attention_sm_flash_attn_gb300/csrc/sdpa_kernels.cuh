@@ -131,7 +131,7 @@ struct AttnParams {
 //            operand from TMEM), one S buffer and P in shared memory.
 enum Mode : int { kSingle = 0, kPair = 1, kDuo = 2, kDuoQ = 3 };
 
-template <bool BF16, int MODE, int HD = 256, int HDV = HD>
+template <bool BF16, int MODE, int HD = 256, int HDV = HD, bool BIAS = false>
 struct Cfg {
   static constexpr bool PAIR = MODE == kPair;
   static constexpr bool DUO = MODE == kDuo || MODE == kDuoQ;
@@ -162,8 +162,14 @@ struct Cfg {
   // other variants keep Q in shared memory, two S buffers, and P in TMEM over
   // the S buffer it came from.
   static constexpr bool QTM = MODE == kDuoQ;
+  // Epilogue through shared memory (STAGE, kDuoQ, in its P buffer): each warp
+  // stages 32 rows x 64 columns of the output and writes whole 128-byte lines.
+  // (The same staging in the other 2-SM kernel, in a buffer of its own,
+  // measured no faster on the sliding-window prefill, so it keeps direct
+  // stores and its smaller shared-memory footprint.)
+  static constexpr bool STAGE = QTM;
   static constexpr int P_OFF = RING_OFF + NSLOT * SLOT;
-  static constexpr int P_BYTES = QTM ? BM * BN * 2 : 0;
+  static constexpr int P_BYTES = STAGE ? BM * BN * 2 : 0;
   static constexpr int X_OFF = P_OFF + P_BYTES;      // peer's partial scores (received)
   static constexpr int X_BYTES = PAIR ? BM * BN * 4 : 0;
   static constexpr int XS_OFF = X_OFF + X_BYTES;     // own partial scores (staged to send)
@@ -195,6 +201,8 @@ struct Cfg {
   static constexpr int kPFullArrivals = DUO ? 16 : 8;
   static_assert(S_COL + NSBUF * BN + (QTM ? DH / 2 : 0) <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(!STAGE || (P_BYTES >= 8 * 4096 && DV == 256 && !PAIR),
+                "the staged epilogue: 8 warps x 32 rows x 64 columns in the P buffer");
   static_assert(KSUB * KBOX * 64 == DH && VSUB * VROWS == BN, "tile decomposition");
   static_assert(VBOX * 64 == (DUO ? DV / 2 : DV) && V_SLOT_BYTES <= SLOT && K_SLOT_BYTES == SLOT,
                 "K/V slot layout");
@@ -530,7 +538,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
 // without it never read p.bias.
 template <bool BF16, int MODE, int HD, int HDV, bool BIAS = false>
 __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
-  using C = Cfg<BF16, MODE, HD, HDV>;
+  using C = Cfg<BF16, MODE, HD, HDV, BIAS>;
   constexpr bool PAIR = C::PAIR;
   constexpr bool DUO = C::DUO;
   constexpr bool CLUSTER = PAIR || DUO;
@@ -542,7 +550,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
   const uint32_t sRing = sbase + C::RING_OFF;
   const uint32_t sX = sbase + C::X_OFF;
   const uint32_t sBar = sbase + C::BAR_OFF;
-  const uint32_t sP = sbase + C::P_OFF;  // P (Q in TMEM only)
+  const uint32_t sP = sbase + C::P_OFF;  // P (Q in TMEM) / epilogue staging
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::BAR_OFF + 240);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 244);
   float* red = reinterpret_cast<float*>(smem + C::RED_OFF);
@@ -1381,7 +1389,47 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
               o[4 * g + 3] = fmaf(ak, v.w, o[4 * g + 3]);
             }
           }
-          if (row_valid) {
+          if constexpr (C::STAGE) {
+            // Through this warp's 4 KB slice of the P buffer (with Q in TMEM, P's
+            // last product has completed; otherwise the buffer holds nothing
+            // else): 32 rows x 64 columns a round, written row-wise and
+            // read back so that one global store covers four whole 128-byte
+            // lines.  Chunk c of slice row r sits at 16-byte position c ^ (r & 7).
+            const uint32_t slice = sP + static_cast<uint32_t>(warp) * 4096u;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              uint4 v;
+              v.x = pack2(o[8 * g + 0] * inv, o[8 * g + 1] * inv, BF16);
+              v.y = pack2(o[8 * g + 2] * inv, o[8 * g + 3] * inv, BF16);
+              v.z = pack2(o[8 * g + 4] * inv, o[8 * g + 5] * inv, BF16);
+              v.w = pack2(o[8 * g + 6] * inv, o[8 * g + 7] * inv, BF16);
+              const int cc = (cch & 1) * 4 + g;
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                               slice + lane * 128 + ((cc ^ (lane & 7)) << 4)),
+                           "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                           : "memory");
+            }
+            if (cch & 1) {
+              __syncwarp();
+              const int colr = col - 32;  // first column of this 64-column round
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const int rr = 4 * k + (lane >> 3);  // slice row
+                const int c = lane & 7;
+                uint4 v;
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                             : "r"(slice + rr * 128 + ((c ^ (rr & 7)) << 4))
+                             : "memory");
+                const int i = w.m0 + q4 * 32 + rr;  // query row of slice row rr
+                if (i < p.Lq) {
+                  const long long rid = (static_cast<long long>(w.b) * p.Hq + w.h0) * p.Lq + i;
+                  *reinterpret_cast<uint4*>(p.out + rid * p.D + d0 + colr + c * 8) = v;
+                }
+              }
+              __syncwarp();  // the slice is rewritten by the next round
+            }
+          } else if (row_valid) {
             uint4* dst = reinterpret_cast<uint4*>(p.out + row_id * p.D + d0 + col);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {

@@ -47,20 +47,20 @@ int ensure_attr(DeviceState* st) {
   if (st->attr_set[idx]) return SDPA_OK;
   auto kern = gbsdpa::attn_fwd_kernel<BF16, MODE, HD, HDV, BIAS>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg<BF16, MODE, HD, HDV>::SMEM_BYTES) != cudaSuccess)
+                           Cfg<BF16, MODE, HD, HDV, BIAS>::SMEM_BYTES) != cudaSuccess)
     return SDPA_ERR_CUDA;
   st->attr_set[idx] = true;
   return SDPA_OK;
 }
 
-template <bool BF16, int MODE, int HD, int HDV>
+template <bool BF16, int MODE, int HD, int HDV, bool BIAS>
 void fill_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, long long ctas,
                  cudaStream_t stream) {
   constexpr bool kCluster = MODE != gbsdpa::kSingle;
   *cfg = {};
   cfg->gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
-  cfg->blockDim = dim3(Cfg<BF16, MODE, HD, HDV>::NTHREADS, 1, 1);
-  cfg->dynamicSmemBytes = Cfg<BF16, MODE, HD, HDV>::SMEM_BYTES;
+  cfg->blockDim = dim3(Cfg<BF16, MODE, HD, HDV, BIAS>::NTHREADS, 1, 1);
+  cfg->dynamicSmemBytes = Cfg<BF16, MODE, HD, HDV, BIAS>::SMEM_BYTES;
   cfg->stream = stream;
   cfg->attrs = attr;
   cfg->numAttrs = 0;
@@ -86,7 +86,7 @@ int launch_attn(const AttnParams& p, long long items, cudaStream_t stream, Devic
   // sized to the occupancy limit, so on an otherwise idle GPU all of it is
   // resident; the kernel starts the never-waiting units first, and a wait that
   // still runs out reports a device timeout instead of hanging.
-  fill_launch<BF16, MODE, HD, HDV>(&cfg, attr, ctas, stream);
+  fill_launch<BF16, MODE, HD, HDV, BIAS>(&cfg, attr, ctas, stream);
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, gbsdpa::attn_fwd_kernel<BF16, MODE, HD, HDV, BIAS>, p);
   return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
@@ -104,15 +104,15 @@ int resident_units(DeviceState* st) {
   if (MODE == gbsdpa::kSingle) {
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern,
-                                                      Cfg<BF16, MODE, HD, HDV>::NTHREADS,
-                                                      Cfg<BF16, MODE, HD, HDV>::SMEM_BYTES) !=
+                                                      Cfg<BF16, MODE, HD, HDV, BIAS>::NTHREADS,
+                                                      Cfg<BF16, MODE, HD, HDV, BIAS>::SMEM_BYTES) !=
         cudaSuccess)
       return 0;
     units = per_sm * st->sms;
   } else {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
-    fill_launch<BF16, MODE, HD, HDV>(&cfg, attr, 2 * (st->sms / 2), nullptr);
+    fill_launch<BF16, MODE, HD, HDV, BIAS>(&cfg, attr, 2 * (st->sms / 2), nullptr);
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) return 0;
     units = clusters;
