@@ -161,24 +161,31 @@ def _workspace(nbytes: int, device, workspace):
     return workspace
 
 
+def bias_strides(shape, strides, B, Hq, Lq, Lk):
+    """Element strides (batch, head, query row) the library reads a bias of this
+    shape and these strides with: a size-1 dim broadcasts (stride 0); the shape
+    must broadcast to [B, Hq, Lq, Lk] and the key dim must be dense."""
+    if len(shape) != 4 or shape[3] != Lk:
+        raise ValueError("bias must be 4-D [B or 1, Hq or 1, Lq or 1, Lk]")
+    for n, full in zip(shape[:3], (B, Hq, Lq)):
+        if n not in (1, full):
+            raise ValueError("bias must broadcast to [B, Hq, Lq, Lk]")
+    if Lk > 1 and strides[3] != 1:
+        raise ValueError("bias rows must be contiguous along keys")
+    return tuple(0 if shape[d] == 1 else int(strides[d]) for d in range(3))
+
+
 def _bias_args(bias, q, B, Hq, Lq, Lk):
     """(pointer, stride_b, stride_h, stride_q) of a bias broadcastable to [B, Hq,
-    Lq, Lk]; size-1 dims broadcast (stride 0), the key dim must be dense."""
+    Lq, Lk] (see bias_strides)."""
     if bias is None:
         return None, 0, 0, 0
     if not bias.is_cuda or bias.device != q.device:
         raise ValueError("bias must be a CUDA tensor on q's device")
     if bias.dtype != q.dtype:
         raise TypeError("bias must have q's dtype")
-    if bias.dim() != 4 or bias.shape[3] != Lk:
-        raise ValueError("bias must be 4-D [B or 1, Hq or 1, Lq or 1, Lk]")
-    for n, full in zip(bias.shape[:3], (B, Hq, Lq)):
-        if n not in (1, full):
-            raise ValueError("bias must broadcast to [B, Hq, Lq, Lk]")
-    if Lk > 1 and bias.stride(3) != 1:
-        raise ValueError("bias rows must be contiguous along keys")
-    st = [0 if bias.shape[d] == 1 else bias.stride(d) for d in range(3)]
-    return bias.data_ptr(), st[0], st[1], st[2]
+    sb, sh, sq = bias_strides(tuple(bias.shape), bias.stride(), B, Hq, Lq, Lk)
+    return bias.data_ptr(), sb, sh, sq
 
 
 def _call(entry, ex_entry, q, k, v, out, B, Hq, Hkv, Lq, Lk, D, Dv, scale, causal, window, lk,

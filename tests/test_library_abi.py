@@ -125,3 +125,30 @@ def test_bias_arguments_are_checked_on_the_host(lib, fn):
     assert call_ex(lib, fn, bias=FAKE, sh=-1, **ok) == -1
     assert call_ex(lib, fn, bias=FAKE, sq=1 << 60, **ok) == -1
     assert call_ex(lib, fn, bias=ctypes.c_void_p(0x10001), sq=3000, **ok) == -6   # odd address
+
+
+def test_bias_strides_broadcast_and_views():
+    import torch
+    B, Hq, Lq, Lk = 2, 4, 9, 40
+    full = torch.zeros(B, Hq, Lq, Lk)
+    assert gb.bias_strides(full.shape, full.stride(), B, Hq, Lq, Lk) == (Hq * Lq * Lk, Lq * Lk, Lk)
+    shared = torch.zeros(1, 1, Lq, Lk)
+    assert gb.bias_strides(shared.shape, shared.stride(), B, Hq, Lq, Lk) == (0, 0, Lk)
+    per_head_row = torch.zeros(B, Hq, 1, Lk)
+    assert gb.bias_strides(per_head_row.shape, per_head_row.stride(), B, Hq, Lq, Lk) == \
+        (Hq * Lk, Lk, 0)
+    # a [.., :Lk] view of wider rows keeps the wider row stride
+    wide = torch.zeros(1, Hq, Lq, Lk + 3)[..., :Lk]
+    assert gb.bias_strides(wide.shape, wide.stride(), B, Hq, Lq, Lk) == (0, Lq * (Lk + 3), Lk + 3)
+    # an expanded tensor: stride 0 where it was expanded
+    exp = torch.zeros(1, 1, 1, Lk).expand(B, Hq, Lq, Lk)
+    assert gb.bias_strides(exp.shape, exp.stride(), B, Hq, Lq, Lk) == (0, 0, 0)
+
+
+@pytest.mark.parametrize("shape,strides", [((1, 1, 1, 39), (39, 39, 39, 1)),
+                                           ((3, 1, 1, 40), (40, 40, 40, 1)),
+                                           ((1, 1, 9, 40), (360, 360, 1, 9)),
+                                           ((1, 40), (40, 1))])
+def test_bias_strides_reject_bad_layouts(shape, strides):
+    with pytest.raises(ValueError):
+        gb.bias_strides(shape, strides, 2, 4, 9, 40)
