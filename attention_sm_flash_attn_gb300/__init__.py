@@ -214,38 +214,52 @@ def _out(q, v, out):
     return out
 
 
+def _checked(out, stream, check, name):
+    """With check=True: synchronise the stream and raise if a kernel reported a
+    device-side failure (its output is then unspecified)."""
+    if check:
+        status, detail = device_status(stream)
+        if status != 0:
+            raise SdpaError(status, f"{name} (device code {detail:#x})")
+    return out
+
+
 def sdpa_prefill(q, k, v, out=None, *, scale=None, causal=False, window=0, workspace=None,
-                 stream=None, lk=None, ring=False, bias=None):
+                 stream=None, lk=None, ring=False, bias=None, check=False):
     """Fused attention over [B, H, L, D] fp16/bf16 CUDA tensors (see sdpa_prefill and
     sdpa_prefill_ex in include/sdpa_gb300.h).  Returns ``out``.  ``workspace`` may
     be a uint8 CUDA tensor; when None one is allocated with torch if the schedule
     wants it.  v may have its own head dim (Q/K 192 with V 256).  With ``lk``
     given (or ``ring``), k and v are a K/V cache of k.shape[2] rows holding
     Lk = lk keys.  ``bias`` (q's dtype, [B or 1, Hq or 1, Lq or 1, Lk], dense along
-    keys) is added to the scaled scores; -inf hides a key."""
+    keys) is added to the scaled scores; -inf hides a key.  ``check=True``
+    synchronises and raises SdpaError if a kernel reported a device-side failure
+    (see sdpa_device_status); otherwise call device_status() yourself."""
     out = _out(q, v, out)
     B, Hq, Hkv, Lq, Lk, D, Dv = _check(q, k, v, out, lk)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     need = prefill_workspace_bytes(B, Hq, Hkv, Lq, Lk, D, causal, window)
     workspace = _workspace(need, q.device, workspace)
-    return _call("sdpa_prefill", "sdpa_prefill_ex", q, k, v, out, B, Hq, Hkv, Lq, Lk, D, Dv,
-                 scale, causal, window, lk, ring, workspace, stream, bias)
+    _call("sdpa_prefill", "sdpa_prefill_ex", q, k, v, out, B, Hq, Hkv, Lq, Lk, D, Dv,
+          scale, causal, window, lk, ring, workspace, stream, bias)
+    return _checked(out, stream, check, "sdpa_prefill")
 
 
 def sdpa_decode(q, k, v, out=None, *, scale=None, causal=True, window=0, workspace=None,
-                stream=None, lk=None, ring=False, bias=None):
+                stream=None, lk=None, ring=False, bias=None, check=False):
     """Split-KV decode / verify for 1 <= Lq <= 8 (see sdpa_decode and sdpa_decode_ex
-    in include/sdpa_gb300.h).  Returns ``out``.  Head dims, ``lk``, ``ring`` and
-    ``bias`` as for sdpa_prefill."""
+    in include/sdpa_gb300.h).  Returns ``out``.  Head dims, ``lk``, ``ring``,
+    ``bias`` and ``check`` as for sdpa_prefill."""
     out = _out(q, v, out)
     B, Hq, Hkv, Lq, Lk, D, Dv = _check(q, k, v, out, lk)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     need = decode_workspace_bytes(B, Hq, Hkv, Lq, Dv)
     workspace = _workspace(need, q.device, workspace)
-    return _call("sdpa_decode", "sdpa_decode_ex", q, k, v, out, B, Hq, Hkv, Lq, Lk, D, Dv,
-                 scale, causal, window, lk, ring, workspace, stream, bias)
+    _call("sdpa_decode", "sdpa_decode_ex", q, k, v, out, B, Hq, Hkv, Lq, Lk, D, Dv,
+          scale, causal, window, lk, ring, workspace, stream, bias)
+    return _checked(out, stream, check, "sdpa_decode")
 
 
 def device_status(stream=None):

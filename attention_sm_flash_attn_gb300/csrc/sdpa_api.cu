@@ -654,6 +654,29 @@ int sdpa_selftest_timeout(const void* q, const void* k, const void* v, void* out
                           sdpa_stream_t stream, int* detail) {
   if (detail) *detail = 0;
   if (!q || !k || !v || !out || (D != 256 && D != 512)) return SDPA_ERR_INVALID_ARG;
+  if (decode == 2) {
+    // Persistent prefill whose suffix pieces never publish their flags: the
+    // prefix units' bounded waits run out and their tiles are stored as NaN.
+    const int B = 1, Hq = 2, Hkv = 1, Lq = 256, Lk = 4096;
+    if (D != 256) return SDPA_ERR_INVALID_ARG;
+    int rc = validate(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, 1.f / 16.f, 1, 0, SDPA_F16);
+    if (rc) return rc;
+    DeviceState* st = nullptr;
+    rc = device_state(&st);
+    if (rc) return rc;
+    const int mode = choose_mode(false, D, 0);
+    const long long u = persistent_units<false>(st, mode, D, B, Hq, Lq, Lk, 1, 0);
+    if (u <= 0) return SDPA_ERR_UNSUPPORTED;
+    if (plan_tail(u, B, Hq, Lq, Lk, 1, 0, key_tile(mode), qtile_rows(mode)).US <= 0)
+      return SDPA_ERR_UNSUPPORTED;  // no suffix pieces on this device: nothing to withhold
+    if (!workspace || workspace_bytes < sk_layout(u).bytes || !aligned16(workspace))
+      return SDPA_ERR_WORKSPACE;
+    rc = run<false>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, 1.f / 16.f, 1, 0, false, 1, false,
+                    workspace, reinterpret_cast<cudaStream_t>(stream), st, /*withhold=*/2, u);
+    if (rc) return rc;
+    return sdpa_device_status(stream, detail);
+  }
+  if (decode != 0 && decode != 1) return SDPA_ERR_INVALID_ARG;
   const int B = 1, Hq = 2, Hkv = 1, Lq = decode ? 1 : 128, Lk = 128;
   int rc = validate(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, 1.f / 16.f, 1, 0, SDPA_F16);
   if (rc) return rc;

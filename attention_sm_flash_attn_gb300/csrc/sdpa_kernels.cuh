@@ -89,7 +89,9 @@ struct AttnParams {
   int write_partial;
   // Self-test only (always 0 on the normal entry points): 1 = withhold the
   // "query tile ready" signal, so the MMA issuer's bounded wait runs out and the
-  // kernel reports a device timeout instead of computing.
+  // kernel reports a device timeout instead of computing; 2 = suffix pieces of
+  // the persistent schedule never publish their flags, so the prefix units'
+  // bounded waits run out.
   int withhold_q;
   // K/V rows: key j is row j of its (b, kv head) plane, or, for a ring buffer of
   // kv_ring rows (a multiple of 128), row j mod kv_ring.
@@ -661,7 +663,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
         if (count == 0) continue;
         const int bh_q = w.b * p.Hq + w.h0;
         const int bh_kv = w.b * p.Hkv + w.hkv;
-        if (!p.decode && !p.withhold_q) {
+        if (!p.decode && p.withhold_q != 1) {
           // The query buffer is free once the previous piece's last S has completed.
           if (issued_q > 0 && !wait_bar(bar(kBarQFree), (issued_q - 1) & 1, abort_flag, p.status,
                                         kDevTimeoutQ)) {
@@ -992,7 +994,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
           }
           ptx::fence_proxy_async_smem();
           asm volatile("bar.sync 1, 256;" ::: "memory");
-          if (threadIdx.x == 0 && !p.withhold_q) ptx::mbar_arrive(bar(kBarQ));
+          if (threadIdx.x == 0 && p.withhold_q != 1) ptx::mbar_arrive(bar(kBarQ));
         }
       }
 
@@ -1323,7 +1325,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
                             __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
         }
         asm volatile("bar.sync 1, 256;" ::: "memory");
-        if (threadIdx.x == 0) {
+        if (threadIdx.x == 0 && p.withhold_q != 2) {
           __threadfence();
           asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p.sk_flag + pc.slot * 2 + rank),
                        "l"(p.epoch)
@@ -1332,7 +1334,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
       } else if (count > 0) {
         // Whole query tile (kind 0) or prefix (kind 1): merge the suffix shares,
         // if any, in key order, then normalise and store.
-        const int n_contrib = pc.kind == 1 ? pc.n_contrib : 0;
+        int n_contrib = pc.kind == 1 ? pc.n_contrib : 0;
         if (n_contrib > 0) {
           if (threadIdx.x == 0) {
             for (int k = 0; k < n_contrib; ++k) {
@@ -1352,6 +1354,11 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
           }
           asm volatile("bar.sync 1, 256;" ::: "memory");
         }
+        // A wait for the suffix shares that gave up (or any other abort of this
+        // CTA) leaves them unknown: merge nothing and store NaN rows, so that a
+        // caller who skips the status check cannot take the tile for a result.
+        const bool poisoned = n_contrib > 0 && *abort_flag != 0;
+        if (poisoned) n_contrib = 0;
         // Combined max and sum (fixed order: own share, then units in order).
         float mtot = m_run;
         for (int k = 0; k < n_contrib; ++k) {
@@ -1364,7 +1371,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
           const float2 mlk = __ldcg(reinterpret_cast<const float2*>(p.sk_ml) + sk_row(pc.slot + k));
           if (mlk.y > 0.f) ltot += ptx::ex2(mlk.x - mtot) * mlk.y;
         }
-        const float inv = ltot > 0.f ? 1.f / ltot : 0.f;
+        const float inv = poisoned ? __int_as_float(0x7fc00000) : (ltot > 0.f ? 1.f / ltot : 0.f);
 #pragma unroll 1
         for (int cch = 0; cch < C::DV / 64; ++cch) {
           const int col = half * (C::DV / 2) + cch * 32;

@@ -97,7 +97,12 @@ enum sdpa_status {
  *   CTAs and merge them in a second kernel.  Either keeps all SMs busy when the
  *   query tiles do not fill whole waves.  A workspace must not be used by two
  *   calls that can run at the same time.
- * Returns SDPA_OK or a negative sdpa_status.
+ * Returns SDPA_OK or a negative sdpa_status.  The return value covers argument
+ * checks and launches only: call sdpa_device_status() to learn whether the
+ * kernels completed.  In the persistent schedule a unit waits (at most 2 s)
+ * for the partials of its tile's tail from other units; if that wait gives up
+ * (for example because other work on the GPU kept those units from running),
+ * the tile's rows are stored as NaN and the status reports 0x10a.
  */
 int sdpa_prefill(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
                  int Lq, int Lk, int D, float scale, int causal, int window, int dtype,
@@ -234,6 +239,15 @@ int sdpa_version(void);
  * it.  No fault, trap or hang is involved; the CUDA context stays usable.
  * q, k, v, out: device buffers of the shapes above ([1,2,Lq,D], [1,1,128,D]);
  * decode also needs a workspace of sdpa_decode_workspace_bytes(1, 2, 1, 1, D).
+ *
+ * decode = 2 tests the persistent prefill schedule instead: D = 256, Lq = 256,
+ * Lk = 4096 (q [1,2,256,256], k and v [1,1,4096,256]) with a workspace of
+ * sdpa_prefill_workspace_bytes(1, 2, 1, 256, 4096, 256, 1, 0) bytes.  The
+ * pieces that compute the tail of a query tile's key range never publish
+ * their "partials ready" flags, so each unit that owns such a tile gives up
+ * its bounded wait for them (code 0x10a), merges nothing and stores NaN rows
+ * for that tile.  SDPA_ERR_UNSUPPORTED if the device's schedule has no such
+ * pieces for this shape.
  */
 int sdpa_selftest_timeout(const void* q, const void* k, const void* v, void* out, int D,
                           int decode, void* workspace, size_t workspace_bytes,

@@ -125,3 +125,40 @@ def test_persistent_and_per_tile_launch_agree():
     for out in (a, b):
         got = out.reshape(-1, D)[sel].double().cpu().numpy()
         assert float(np.max(np.abs(got - ref))) < TOL[torch.bfloat16]
+
+
+@pytest.mark.parametrize("rep", range(3))
+def test_persistent_prefill_under_contention(rep):
+    """The persistent grid is sized to the occupancy limit and its units wait
+    (bounded) on one another.  Here cuBLAS GEMMs on another stream hold the SMs
+    while the prefill is queued, so its units become resident piecemeal.  The
+    call must either match the oracle or report the timeout through the device
+    status, never return wrong numbers with a clean status."""
+    B, Hq, Hkv, Lq, Lk, causal, window = CASES[0]
+    D = 256
+    q, k, v = draw(B, Hq, Hkv, Lq, Lk, D, torch.float16, seed=31 + rep)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    need = gb.prefill_workspace_bytes(B, Hq, Hkv, Lq, Lk, D, causal, window)
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    out = torch.empty_like(qd)
+    n = 4096 + 2048 * rep
+    a = torch.randn(n, n, device=DEV, dtype=torch.bfloat16)
+    side = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(side):
+        for _ in range(6):
+            a = (a @ a) * (1.0 / n)
+    gb.sdpa_prefill(qd, kd, vd, out, causal=causal, window=window, workspace=ws)
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            a = (a @ a) * (1.0 / n)
+    torch.cuda.synchronize()
+    status, detail = gb.device_status()
+    ids = rows_to_check(B, Hq, Lq, seed=5 + rep)
+    got = out.reshape(-1, D)[torch.as_tensor(ids, device=DEV)].double().cpu().numpy()
+    if status != 0:
+        assert detail == 0x10a, hex(detail)
+        assert np.isnan(got).any()
+        return
+    ref = oracle.sdpa(q, k, v, causal=causal, window=window, rows=ids)
+    assert float(np.max(np.abs(got - ref))) < TOL[torch.float16]

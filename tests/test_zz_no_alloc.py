@@ -7,17 +7,20 @@ no-alloc entry point keeps its split partials in a scratch array that is part
 of the library itself.  These tests call it through the C ABI and check it
 against the regular sdpa_decode entry point (same tolerance as the other GPU
 parity tests; the two share the kernels, so they also agree bit for bit), on
-two calls in a row, and check that an oversized call is refused cleanly.
+two calls in a row, compare the second call with the fp64 oracle, and check
+that an oversized call is refused cleanly.
 
 The file is named so that pytest collects it last.
 """
 import ctypes
 import math
 
+import numpy as np
 import pytest
 import torch
 
 import attention_sm_flash_attn_gb300 as gb
+import oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -61,6 +64,10 @@ def test_noalloc_matches_decode_on_two_calls_in_a_row(case):
         err = float((got.float() - want.float()).abs().max())
         assert err < TOL[dtype], (call, err)
         assert torch.equal(got, want), call
+    # the last call against the fp64 oracle as well
+    ref = oracle.sdpa(q.cpu(), k.cpu(), v.cpu(), causal=True, window=window)
+    err = float(np.max(np.abs(got.cpu().double().numpy() - ref)))
+    assert err < TOL[dtype], err
 
 
 def test_noalloc_rejects_calls_beyond_its_scratch():
