@@ -178,10 +178,12 @@ size_t partial_bytes(long long R, int D, int n_splits) {
 // window shorter than 256 keys, where most of a 256-row tile's keys would be
 // masked; head_dim 192 prefill stays on one CTA (the 2-SM tile would split V
 // into 96-column halves, which a 128-byte-swizzled 64-column box cannot hold);
-// decode uses one CTA per 16 query heads x 8 position slots.
+// decode uses one CTA per 16 query heads x 8 position slots and split, the
+// splits of a head group forming a cluster (kDecode) below head_dim 512.
 int choose_mode(bool decode, int D, int window) {
   if (D == 512) return gbsdpa::kPair;
-  if (decode || D == 192) return gbsdpa::kSingle;
+  if (decode) return gbsdpa::kDecode;
+  if (D == 192) return gbsdpa::kSingle;
   return (window > 0 && window < 256) ? gbsdpa::kSingle : gbsdpa::kDuo;
 }
 
@@ -197,7 +199,7 @@ int launch_mode(int mode, int D, int Dv, int window, bool bias) {
 
 bool two_sm(int mode) { return mode == gbsdpa::kDuo || mode == gbsdpa::kDuoQ; }
 int qtile_rows(int mode) { return two_sm(mode) ? 256 : 128; }
-int key_tile(int mode) { return mode == gbsdpa::kPair ? 64 : 128; }
+int key_tile(int mode) { return (mode == gbsdpa::kPair || mode == gbsdpa::kDecode) ? 64 : 128; }
 
 // Key tiles the longest query tile (of `rows` rows) visits.
 long long max_tiles_per_qtile(int Lq, int Lk, int causal, int window, int bn, int rows) {
@@ -253,6 +255,55 @@ int plan_decode_splits(int sms, int B, int Hq, int Hkv, int D, int window = 0) {
   }
   s = std::max<long long>(1, std::min<long long>(s, 256));
   return static_cast<int>(s);
+}
+
+// Decode split plan.  S splits per (batch, kv head, head block) group deal the
+// group's key tiles round-robin.  kDecode (head dim <= 256): the splits are NC
+// clusters of CS CTAs (S = CS * NC); a cluster merges its splits through
+// distributed shared memory, so with one cluster per group a single launch
+// writes the output and needs no workspace.  Everything here depends on
+// (B, Hq, Hkv, D, window) and the device only, never on Lq or Lk: the split a
+// tile goes to, and so every row's arithmetic, is the same for a verify call
+// and the single-row call over its trimmed keys.
+struct DecodePlan {
+  int S = 1, CS = 0, NC = 1;  // CS = 0: not a cluster plan (head-dim-split pair)
+};
+
+long long decode_groups(int B, int Hq, int Hkv) {
+  return static_cast<long long>(B) * Hkv * ((Hq / Hkv + 15) / 16);
+}
+
+DecodePlan plan_decode(DeviceState* st, int B, int Hq, int Hkv, int D, int Dv, int window) {
+  DecodePlan pl;
+  if (choose_mode(true, D, 0) != gbsdpa::kDecode) {
+    pl.S = plan_decode_splits(st->sms, B, Hq, Hkv, D, window);
+    return pl;
+  }
+  const long long groups = decode_groups(B, Hq, Hkv);
+  // 64-key tiles the rows of a group can see: at most window + 7 keys (Lq <= 8).
+  const long long t_max = window > 0 ? (window + 6 + 63) / 64 + 1 : (1ll << 30);
+  const long long cap = std::min<long long>(
+      {gbsdpa::kMaxDecodeClusterCtas, t_max, std::max<long long>(1, st->sms / groups)});
+  // The largest power-of-two cluster whose clusters for all groups can be
+  // resident at once (a second wave would double the latency).
+  int cs = 1;
+  while (cs * 2 <= cap) cs *= 2;
+  for (; cs > 1; cs /= 2)
+    if (gbsdpa_host::decode_fit(D, Dv, st, cs) >= groups) break;
+  const int fit = std::max(1, gbsdpa_host::decode_fit(D, Dv, st, cs));
+  long long nc = std::min<long long>(st->sms / (groups * cs), t_max / cs);
+  nc = std::min<long long>(nc, fit / std::max<long long>(1, groups));
+  pl.CS = cs;
+  pl.NC = static_cast<int>(std::max<long long>(1, std::min<long long>(nc, 64)));
+  pl.S = pl.CS * pl.NC;
+  return pl;
+}
+
+// Workspace of a decode call with this plan: the fp32 partials the combine
+// kernel merges (0 when the clusters write the output).
+size_t decode_partial_bytes(const DecodePlan& pl, long long R, int Dv) {
+  if (pl.CS > 0) return pl.NC > 1 ? partial_bytes(R, Dv, pl.NC) : 0;
+  return partial_bytes(R, Dv, pl.S);
 }
 
 // ----------------------------------------------------------- persistent plan
@@ -364,14 +415,29 @@ int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, i
         int Lk, int D, float scale, int causal, int window, bool decode, int n_splits,
         bool write_partial, void* workspace, cudaStream_t stream, DeviceState* st,
         int withhold_q = 0, long long sk_units = 0, int kv_cap = 0, int kv_ring = 0, int Dv = 0,
-        const BiasArg& bias = BiasArg()) {
-  // D is the Q/K head dim; Dv (0: the same) is V's and the output's.
+        const BiasArg& bias = BiasArg(), const DecodePlan* dplan = nullptr) {
+  // D is the Q/K head dim; Dv (0: the same) is V's and the output's.  Decode
+  // takes its split plan from `dplan` (n_splits / write_partial are ignored).
   if (Dv <= 0) Dv = D;
   AttnParams p;
   std::memset(&p, 0, sizeof(p));
   const int mode = choose_mode(decode, D, window);
-  // K boxes: all keys of a tile (one CTA), or the CTA's 64 keys (pair kernels);
-  // V boxes: 32 keys (one CTA, head-dim split) or 64 keys (2-SM MMA).
+  int n_partials = n_splits;  // fp32 partials per row for the combine kernel
+  if (mode == gbsdpa::kDecode) {
+    if (!dplan || dplan->CS < 1) return SDPA_ERR_INVALID_ARG;
+    n_splits = dplan->S;
+    n_partials = dplan->NC;
+    write_partial = dplan->NC > 1;
+    p.dec_cs = dplan->CS;
+    p.dec_nc = dplan->NC;
+  } else if (decode) {
+    if (!dplan) return SDPA_ERR_INVALID_ARG;
+    n_splits = n_partials = dplan->S;
+    write_partial = true;
+  }
+  // K boxes: all keys of a tile (one CTA, 128-key tiles), or 64 keys (pair
+  // kernels, decode); V boxes: 32 keys (one CTA, head-dim split) or 64 keys
+  // (2-SM MMA).
   const int k_rows = mode == gbsdpa::kSingle ? 128 : 64;
   const int v_rows = two_sm(mode) ? 64 : 32;
   int rc = SDPA_OK;
@@ -390,7 +456,7 @@ int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, i
   p.q = static_cast<const uint16_t*>(q);
   p.out = static_cast<uint16_t*>(out);
   if (write_partial) {
-    const size_t po = static_cast<size_t>(n_splits) * static_cast<size_t>(R) * Dv * sizeof(float);
+    const size_t po = static_cast<size_t>(n_partials) * static_cast<size_t>(R) * Dv * sizeof(float);
     p.part_o = static_cast<float*>(workspace);
     p.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                          ((po + 255) & ~static_cast<size_t>(255)));
@@ -450,7 +516,7 @@ int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, i
               : gbsdpa_host::launch_variant<BF16, false>(lm, D, Dv, p, items, stream, st);
   if (rc) return rc;
   if (write_partial)
-    rc = launch_combine(p.part_o, p.part_ml, out, R, Dv, n_splits, BF16, stream);
+    rc = launch_combine(p.part_o, p.part_ml, out, R, Dv, n_partials, BF16, stream);
   return rc;
 }
 
@@ -498,8 +564,10 @@ size_t sdpa_decode_workspace_bytes(int B, int Hq, int Hkv, int Lq, int D) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lq > 8 || Hq % Hkv) return 0;
   if (!supported_head_dim(D)) return 0;
   if (device_state(&st)) return 0;
-  const int s = plan_decode_splits(st->sms, B, Hq, Hkv, D);
-  return partial_bytes(static_cast<long long>(B) * Hq * Lq, D, s);
+  // The plan without a window: a window never needs more (it can only cut the
+  // cluster size, and then to one cluster per group).
+  const long long R = static_cast<long long>(B) * Hq * Lq;
+  return decode_partial_bytes(plan_decode(st, B, Hq, Hkv, D, D, 0), R, D);
 }
 
 static int prefill_impl(const void* q, const void* k, const void* v, void* out, int B, int Hq,
@@ -555,20 +623,19 @@ static int decode_impl(const void* q, const void* k, const void* v, void* out, i
   rc = validate_bias(bias);
   if (rc) return rc;
   if (Lq > 8) return SDPA_ERR_INVALID_ARG;
-  if (!workspace) return SDPA_ERR_WORKSPACE;
-  if (!aligned16(workspace)) return SDPA_ERR_ALIGNMENT;
+  if (workspace && !aligned16(workspace)) return SDPA_ERR_ALIGNMENT;
   DeviceState* st = nullptr;
   rc = device_state(&st);
   if (rc) return rc;
-  const int s = plan_decode_splits(st->sms, B, Hq, Hkv, D, causal ? window : 0);
-  if (workspace_bytes < partial_bytes(static_cast<long long>(B) * Hq * Lq, Dv, s))
-    return SDPA_ERR_WORKSPACE;
   const bool bf16 = dtype == SDPA_BF16;
+  const DecodePlan pl = plan_decode(st, B, Hq, Hkv, D, Dv, causal ? window : 0);
+  const size_t need = decode_partial_bytes(pl, static_cast<long long>(B) * Hq * Lq, Dv);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return SDPA_ERR_WORKSPACE;
   auto strm = reinterpret_cast<cudaStream_t>(stream);
-  return bf16 ? run<true>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, true, s,
-                          true, workspace, strm, st, 0, 0, kv_cap, kv_ring, Dv, bias)
-              : run<false>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, true, s,
-                           true, workspace, strm, st, 0, 0, kv_cap, kv_ring, Dv, bias);
+  return bf16 ? run<true>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, true, 0,
+                          true, workspace, strm, st, 0, 0, kv_cap, kv_ring, Dv, bias, &pl)
+              : run<false>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, true, 0,
+                           true, workspace, strm, st, 0, 0, kv_cap, kv_ring, Dv, bias, &pl);
 }
 
 int sdpa_prefill(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
@@ -684,14 +751,15 @@ int sdpa_selftest_timeout(const void* q, const void* k, const void* v, void* out
   rc = device_state(&st);
   if (rc) return rc;
   auto strm = reinterpret_cast<cudaStream_t>(stream);
-  int s = 1;
+  DecodePlan pl;
   if (decode) {
-    s = plan_decode_splits(st->sms, B, Hq, Hkv, D);
-    if (!workspace || workspace_bytes < partial_bytes(static_cast<long long>(B) * Hq * Lq, D, s))
-      return SDPA_ERR_WORKSPACE;
+    pl = plan_decode(st, B, Hq, Hkv, D, D, 0);
+    const size_t need = decode_partial_bytes(pl, static_cast<long long>(B) * Hq * Lq, D);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return SDPA_ERR_WORKSPACE;
   }
-  rc = run<false>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, 1.f / 16.f, 1, 0, decode != 0, s,
-                  decode != 0, workspace, strm, st, /*withhold_q=*/1);
+  rc = run<false>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, 1.f / 16.f, 1, 0, decode != 0, 1, false,
+                  workspace, strm, st, /*withhold_q=*/1, 0, 0, 0, 0, BiasArg(),
+                  decode ? &pl : nullptr);
   if (rc) return rc;
   return sdpa_device_status(stream, detail);
 }
@@ -736,16 +804,17 @@ extern "C" int sdpa_decode_noalloc(const void* q, const void* k, const void* v, 
   DeviceState* st = nullptr;
   rc = device_state(&st);
   if (rc) return rc;
-  const int s = plan_decode_splits(st->sms, B, Hq, Hkv, D, causal ? window : 0);
-  if (partial_bytes(static_cast<long long>(B) * Hq * Lq, D, s) > SDPA_NOALLOC_SCRATCH_BYTES)
+  const bool bf16 = dtype == SDPA_BF16;
+  const DecodePlan pl = plan_decode(st, B, Hq, Hkv, D, D, causal ? window : 0);
+  if (decode_partial_bytes(pl, static_cast<long long>(B) * Hq * Lq, D) >
+      SDPA_NOALLOC_SCRATCH_BYTES)
     return SDPA_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
   rc = noalloc_scratch(&scratch);
   if (rc) return rc;
   auto strm = reinterpret_cast<cudaStream_t>(stream);
-  return dtype == SDPA_BF16
-             ? run<true>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, true, s,
-                         true, scratch, strm, st)
-             : run<false>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, true, s,
-                          true, scratch, strm, st);
+  return bf16 ? run<true>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, true, 0,
+                          true, scratch, strm, st, 0, 0, 0, 0, 0, BiasArg(), &pl)
+              : run<false>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, true, 0,
+                           true, scratch, strm, st, 0, 0, 0, 0, 0, BiasArg(), &pl);
 }

@@ -67,6 +67,7 @@ enum : int {
   kDevTimeoutPair = 0x10a,  // a prefix unit waited too long for a suffix piece's partials
   kDevMisaligned = 0x10b,
   kDevBadCluster = 0x10c,  // a 2-CTA variant was launched without a cluster of 2
+  kDevBadGrid = 0x10d,     // a decode CTA found no work item of the call (grid too large)
 };
 
 struct AttnParams {
@@ -86,6 +87,11 @@ struct AttnParams {
   int n_qtiles;   // prefill: ceil(Lq / 128)
   int n_splits;   // prefill: 1 => final output written directly; decode: fixed split count
   int n_hb;       // decode: query-head blocks of 16 per kv head
+  // kDecode: the n_splits splits of a (batch, kv head, head block) group are
+  // dec_nc clusters of dec_cs CTAs; a cluster merges its splits through
+  // distributed shared memory and writes the output (dec_nc == 1) or one fp32
+  // partial per cluster for the combine kernel (dec_nc > 1).
+  int dec_cs, dec_nc;
   int write_partial;
   // Self-test only (always 0 on the normal entry points): 1 = withhold the
   // "query tile ready" signal, so the MMA issuer's bounded wait runs out and the
@@ -131,23 +137,32 @@ struct AttnParams {
 //            tile, which halves the bytes each SM stages per FLOP.
 //   kDuoQ:   the 2-SM variant with Q in tensor memory (Q.K^T reads its A
 //            operand from TMEM), one S buffer and P in shared memory.
-enum Mode : int { kSingle = 0, kPair = 1, kDuo = 2, kDuoQ = 3 };
+//   kDecode: decode (Lq <= 8) at head_dim <= 256: one CTA per split over
+//            64-key tiles; the splits of a (batch, kv head, head block) form a
+//            thread-block cluster and merge their partials through distributed
+//            shared memory at the end, so one launch writes the output.
+enum Mode : int { kSingle = 0, kPair = 1, kDuo = 2, kDuoQ = 3, kDecode = 4 };
 
 template <bool BF16, int MODE, int HD = 256, int HDV = HD, bool BIAS = false>
 struct Cfg {
   static constexpr bool PAIR = MODE == kPair;
   static constexpr bool DUO = MODE == kDuo || MODE == kDuoQ;
+  static constexpr bool DEC = MODE == kDecode;
   static constexpr int BM = 128;                   // query rows per CTA
   static constexpr int DH = HD;                    // Q/K head-dim columns owned by one CTA
   static constexpr int DV = HDV;                   // V (and output) head-dim columns
-  static constexpr int BN = PAIR ? 64 : 128;       // keys per tile
+  static constexpr int BN = (PAIR || DEC) ? 64 : 128;  // keys per tile
   static constexpr int HB = BN / 2;                // key columns per softmax thread
   static constexpr int NSLOT = PAIR ? 5 : 8;
   static constexpr int SLOT = 16384;
   // K per CTA and tile: DUO holds 64 of the 128 keys, the others all BN keys.
   static constexpr int KROWS = DUO ? 64 : BN;      // rows of a K box
-  static constexpr int KSUB = DH * KROWS * 2 / SLOT;  // K slots per tile
-  static constexpr int KBOX = SLOT / (KROWS * 128);   // 64-column K boxes per slot
+  // 64-column K boxes per slot: as many as fit (two of 64 rows, one of 128),
+  // fewer when the head dim's box count does not divide by that (192 = 3 boxes
+  // of 64 rows go one to a slot).
+  static constexpr int KBOX_FIT = SLOT / (KROWS * 128);
+  static constexpr int KBOX = (DH / 64) % KBOX_FIT == 0 ? KBOX_FIT : 1;
+  static constexpr int KSUB = DH / 64 / KBOX;      // K slots per tile
   // V per CTA and tile: DUO holds 128 of the 256 head-dim columns for all keys,
   // in slots of 64 keys x 128 columns; the others hold slots of 32 keys x 256.
   static constexpr int VROWS = DUO ? 64 : 32;      // keys per V slot (= rows of a V box)
@@ -206,8 +221,9 @@ struct Cfg {
   static_assert(!STAGE || (P_BYTES >= 8 * 4096 && DV == 256 && !PAIR),
                 "the staged epilogue: 8 warps x 32 rows x 64 columns in the P buffer");
   static_assert(KSUB * KBOX * 64 == DH && VSUB * VROWS == BN, "tile decomposition");
-  static_assert(VBOX * 64 == (DUO ? DV / 2 : DV) && V_SLOT_BYTES <= SLOT && K_SLOT_BYTES == SLOT,
+  static_assert(VBOX * 64 == (DUO ? DV / 2 : DV) && V_SLOT_BYTES <= SLOT && K_SLOT_BYTES <= SLOT,
                 "K/V slot layout");
+
   static_assert(Q_BYTES <= RING_OFF && (!PAIR || (DH == 256 && DV == 256)) && DV <= S_COL,
                 "query tile / pair head dim / O columns");
 };
@@ -231,6 +247,10 @@ enum {
 static_assert(kNumBars * 8 <= 240, "barriers end below the TMEM slot and abort flag");
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
+
+// Largest decode cluster (CTAs); 16 is the non-portable cluster size.
+constexpr int kMaxDecodeClusterCtas = 16;
+
 
 // Bounded mbarrier wait.  Gives up after kTimeoutNs (or when another role of
 // this CTA already gave up), records `code` in the device status word and
@@ -294,10 +314,18 @@ __device__ __forceinline__ Work make_work(const AttnParams& p, int item, int ran
     w.t_step = 1;
     w.t_count = max(0, min(per, thi - w.t_begin));
   } else {
-    const int hb = item % p.n_hb;
-    item /= p.n_hb;
-    w.split = item % p.n_splits;
-    item /= p.n_splits;
+    int hb;
+    if (p.dec_cs > 0) {  // kDecode: the splits of one group are consecutive (one cluster each)
+      w.split = item % p.n_splits;
+      item /= p.n_splits;
+      hb = item % p.n_hb;
+      item /= p.n_hb;
+    } else {
+      hb = item % p.n_hb;
+      item /= p.n_hb;
+      w.split = item % p.n_splits;
+      item /= p.n_splits;
+    }
     w.hkv = item % p.Hkv;
     w.b = item / p.Hkv;
     w.h0 = w.hkv * p.G + hb * 16;
@@ -494,6 +522,25 @@ __device__ __forceinline__ bool iter_next(const AttnParams& p, IterState& st, Pi
   return false;
 }
 
+// Next piece of a CTA.  ONE (decode): a single launch-planned piece, without the
+// persistent schedule's code.
+template <int BN, int QROWS, bool ONE>
+__device__ __forceinline__ bool next_piece(const AttnParams& p, IterState& st, Piece& pc) {
+  if constexpr (ONE) {
+    pc.valid = 0;
+    pc.slot = 0;
+    pc.n_contrib = 0;
+    if (st.stage != 4) return false;
+    st.stage = 3;
+    pc.w = make_work<BN, QROWS>(p, st.unit, st.rank);
+    pc.kind = 3;
+    pc.valid = 1;
+    return true;
+  } else {
+    return iter_next<BN, QROWS>(p, st, pc);
+  }
+}
+
 // Bias entries for keys [k0, k0 + N) of one row, as N / 2 packed 16-bit pairs;
 // keys at or past Lk (masked anyway) and rows without a bias (brow null) read 0.
 template <int N>
@@ -566,8 +613,17 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
   }
   // The 2-CTA variants address their peer's shared memory and pair their MMAs:
   // without a cluster of two that would touch memory that is not there.
-  if (CLUSTER && ptx::cluster_nctarank() != 2) {
+  if ((CLUSTER && ptx::cluster_nctarank() != 2) ||
+      (C::DEC && (p.dec_cs < 1 || ptx::cluster_nctarank() != static_cast<uint32_t>(p.dec_cs)))) {
     if (threadIdx.x == 0) atomicCAS(p.status, 0, kDevBadCluster);
+    return;
+  }
+  // Decode: every CTA is one split of one group.  A CTA beyond them (a grid
+  // larger than planned) has nothing to compute and must not address memory;
+  // its whole cluster is beyond them too, so no cluster barrier waits for it.
+  if (C::DEC && static_cast<long long>(blockIdx.x) >=
+                    static_cast<long long>(p.B) * p.Hkv * p.n_hb * p.n_splits) {
+    if (threadIdx.x == 0) atomicCAS(p.status, 0, kDevBadGrid);
     return;
   }
   // A merge kernel queued behind this grid may be placed on SMs as CTAs of this
@@ -591,7 +647,15 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
     return (DUO && rank != 0) ? ptx::mapa(bar(i), 0) : bar(i);
   };
 
-  if (threadIdx.x == 0) {
+  // Barriers are initialised by thread 0, or, in decode, by the producer lane,
+  // which then starts its loads without waiting for the rest of the CTA.
+  const bool init_thread =
+      C::DEC ? (warp == C::kProducerWarp && lane == 0) : (threadIdx.x == 0);
+  if (C::DEC && warp == C::kProducerWarp && lane == 0) {
+    ptx::prefetch_tmap(&p.tm_k);
+    ptx::prefetch_tmap(&p.tm_v);
+  }
+  if (init_thread) {
     ptx::mbar_init(bar(kBarQ), 1);
     for (int s = 0; s < C::NSLOT; ++s) {
       ptx::mbar_init(bar(kBarKvFull + s), 1);
@@ -609,10 +673,67 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
     *abort_flag = 0;
     ptx::fence_mbarrier_init();
   }
-  if (warp == C::kProducerWarp && lane == 0 && !p.decode) {
-    ptx::prefetch_tmap(&p.tm_q);
+  if (!C::DEC && warp == C::kProducerWarp && lane == 0) {
+    if (!p.decode) ptx::prefetch_tmap(&p.tm_q);
     ptx::prefetch_tmap(&p.tm_k);
     ptx::prefetch_tmap(&p.tm_v);
+  }
+  // Decode: ring loads the producer issues right after initialising the
+  // barriers, before the CTA-wide start (the first NSLOT slots need no wait:
+  // each slot is used for the first time).  The producer loop skips them.
+  uint32_t pre_issued = 0;
+  if constexpr (C::DEC) {
+    if (warp == C::kProducerWarp && lane == 0) {
+      const Work w = make_work<C::BN, 128>(p, item, 0);
+      const int bh_kv = w.b * p.Hkv + w.hkv;
+      const int c = w.t_count;
+      // Load units in the producer loop's order: K_0, then (K_j, V_{j-1}) for
+      // j >= 1, then V_{c-1}.
+      for (int u = 0; u < 2 * c && pre_issued < static_cast<uint32_t>(C::NSLOT); ++u) {
+        const bool is_k = u == 0 || (u != 2 * c - 1 && (u & 1));
+        const int j = u == 0 ? 0 : (u == 2 * c - 1 ? c - 1 : (is_k ? (u + 1) / 2 : u / 2 - 1));
+        const int tile_key = (w.t_begin + j * w.t_step) * BN;
+        const int key0 = p.kv_ring ? tile_key % p.kv_ring : tile_key;
+        const int nsub = is_k ? C::KSUB : C::VSUB;
+        for (int sub = 0; sub < nsub && pre_issued < static_cast<uint32_t>(C::NSLOT);
+             ++sub, ++pre_issued) {
+          const uint32_t slot = pre_issued;
+          const uint32_t fb = bar(kBarKvFull + static_cast<int>(slot));
+          ptx::mbar_arrive_expect_tx(fb, is_k ? C::K_SLOT_BYTES : C::V_SLOT_BYTES);
+          if (is_k) {
+            for (int e = 0; e < C::KBOX; ++e)
+              ptx::tma_load_3d(sRing + slot * C::SLOT + e * (C::KROWS * 128), &p.tm_k, fb,
+                               (sub * C::KBOX + e) * 64, key0, bh_kv);
+          } else {
+            for (int cc = 0; cc < C::VBOX; ++cc)
+              ptx::tma_load_3d(sRing + slot * C::SLOT + cc * C::V_LBO, &p.tm_v, fb, cc * 64,
+                               key0 + sub * C::VROWS, bh_kv);
+          }
+        }
+      }
+    }
+  }
+  if constexpr (C::DEC) {
+    // Decode: each softmax thread copies its half of its row's query slice into
+    // the swizzled query tile right away (16-byte chunk c of tile row t at
+    // 16-byte position c ^ (t & 7) of the row's 128-byte line, one 16 KB block
+    // per 64 columns); rows that hold no query row of this call are zeroed.
+    if (warp < 8) {
+      const Work w0 = make_work<C::BN, 128>(p, item, 0);
+      const int t = (warp & 3) * 32 + lane;
+      const int hl = t >> 3;
+      const int i = ((((t & 7) - (p.Lk - p.Lq)) % 8) + 8) % 8;
+      const int h = w0.h0 + hl;
+      const bool valid = (i < p.Lq) && (hl < min(p.G, 16)) && (h < (w0.hkv + 1) * p.G);
+      const long long rid = valid ? (static_cast<long long>(w0.b) * p.Hq + h) * p.Lq + i : 0;
+      const uint16_t* src = p.q + rid * p.Dqk;
+      const int hf = warp >> 2;
+      for (int cq = hf * (C::DH / 16); cq < (hf + 1) * (C::DH / 16); ++cq) {
+        const int dc = cq >> 3, cc = cq & 7;
+        ptx::cp_async_16(sQ + dc * 16384 + t * 128 + ((cc ^ (t & 7)) << 4), src + cq * 8,
+                         valid ? 16u : 0u);
+      }
+    }
   }
   if (warp == C::kMmaWarp) {
     if constexpr (DUO) {
@@ -623,16 +744,33 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
       ptx::tmem_relinquish();
     }
   }
-  ptx::tc_fence_before();
-  __syncthreads();
-  if (CLUSTER) ptx::cluster_sync();  // peer barriers initialised before any remote use
+  if constexpr (C::DEC) {
+    // Named barriers instead of a CTA-wide one, so the producer never waits:
+    // 6 (producer + MMA warps): the barriers are initialised;
+    // 7 (MMA + softmax warps): tensor memory is allocated.
+    if (warp == C::kProducerWarp) {
+      __syncwarp();
+      ptx::bar_arrive(6, 64);
+    } else if (warp == C::kMmaWarp) {
+      ptx::bar_sync(6, 64);
+      ptx::tc_fence_before();
+      ptx::bar_arrive(7, 288);
+    } else if (warp < 8) {
+      ptx::bar_sync(7, 288);
+    }
+  } else {
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (CLUSTER) ptx::cluster_sync();  // peer barriers initialised before any remote use
+  }
   ptx::tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  // (in decode the producer and idle warps never use it and do not wait for it)
+  const uint32_t tmem = (C::DEC && warp >= 8 && warp != C::kMmaWarp) ? 0u : *tmem_slot;
   const bool mma_cta = !DUO || rank == 0;  // this CTA issues MMAs
 
   // Producer / MMA bookkeeping kept for the drain after an abort.
   int issued_q = 0;  // query tiles loaded (one per piece with key tiles)
-  uint32_t ring_issued = 0;  // ring loads issued, in sequence order
+  uint32_t ring_issued = pre_issued;  // ring loads issued, in sequence order
   int mma_issued = 0;
 
   // Warpgroup 2 (producer, MMA issuer, two idle warps) hands its spare
@@ -657,7 +795,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
       IterState& ist = *reinterpret_cast<IterState*>(smem + C::ITER_OFF + 256);
       Piece& pc = *reinterpret_cast<Piece*>(smem + C::ITER_OFF + 256 + 96);
       iter_init<BN, QROWS>(p, ist, item, static_cast<int>(rank));
-      while (ok && iter_next<BN, QROWS>(p, ist, pc)) {
+      while (ok && next_piece<BN, QROWS, C::DEC>(p, ist, pc)) {
         const Work& w = pc.w;
         const int count = w.t_count;
         if (count == 0) continue;
@@ -695,6 +833,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
           const int key0 =
               kv_row((w.t_begin + j * w.t_step) * BN) + (DUO ? static_cast<int>(rank) * 64 : 0);
           for (int ks = 0; ks < C::KSUB && ok; ++ks, ++n) {
+            if (n < pre_issued) continue;  // issued before the CTA-wide start
             int slot;
             uint32_t fb;
             if (!next_slot(slot, fb, C::K_SLOT_BYTES)) {
@@ -712,6 +851,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
           const int key0 = kv_row((w.t_begin + j * w.t_step) * BN);
           const int dv0 = DUO ? static_cast<int>(rank) * (C::DV / 2) : d0;
           for (int vs = 0; vs < C::VSUB && ok; ++vs, ++n) {
+            if (n < pre_issued) continue;  // issued before the CTA-wide start
             int slot;
             uint32_t fb;
             if (!next_slot(slot, fb, C::V_SLOT_BYTES)) {
@@ -859,7 +999,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
       IterState& ist = *reinterpret_cast<IterState*>(smem + C::ITER_OFF + 512);
       Piece& pc = *reinterpret_cast<Piece*>(smem + C::ITER_OFF + 512 + 96);
       iter_init<BN, QROWS>(p, ist, item, static_cast<int>(rank));
-      while (ok && iter_next<BN, QROWS>(p, ist, pc)) {
+      while (ok && next_piece<BN, QROWS, C::DEC>(p, ist, pc)) {
         const int count = pc.w.t_count;
         if (count == 0) continue;
         if (!wait_bar(bar(kBarQ), done_pieces & 1, abort_flag, p.status, kDevTimeoutQ)) {
@@ -895,6 +1035,13 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
         ++done_pieces;
       }
     }
+  }
+  if constexpr (C::DEC) {
+    // The softmax warps' cluster merge: this warpgroup takes part in its two
+    // cluster barriers (every thread of the cluster arrives at each).
+    __syncwarp();
+    ptx::cluster_sync();
+    ptx::cluster_sync();
   }
   } else {
     ptx::setmaxnreg_inc<C::kRegsSoftmax>();
@@ -951,7 +1098,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
     const int unit = item;
     if (threadIdx.x == 0) iter_init<BN, QROWS>(p, *ist, unit, static_cast<int>(rank));
     for (int np = 0;; ++np) {
-      if (threadIdx.x == 0) iter_next<BN, QROWS>(p, *ist, pcs[np & 1]);
+      if (threadIdx.x == 0) next_piece<BN, QROWS, C::DEC>(p, *ist, pcs[np & 1]);
       if (!ptx::bar_red_and(1, 256, ok)) break;
       const Piece& pc = pcs[np & 1];
       if (!pc.valid) break;
@@ -981,16 +1128,21 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
           brow = p.bias + w.b * p.bias_sb + h * p.bias_sh + i * p.bias_sq;
         if (count > 0) {
           // Decode: stage this thread's half of the row's query slice into the
-          // swizzled Q tile (16-byte chunks of 8 elements).
-          const uint4* src = reinterpret_cast<const uint4*>(p.q + row_id * p.Dqk + d0);
-          for (int cq = half * (C::DH / 16); cq < (half + 1) * (C::DH / 16); ++cq) {
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (row_valid) v = src[cq];
-            const int dc = cq >> 3, cc = cq & 7;
-            const uint32_t addr = sQ + dc * 16384 + t * 128 + ((cc ^ (t & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x),
-                         "r"(v.y), "r"(v.z), "r"(v.w)
-                         : "memory");
+          // swizzled Q tile (16-byte chunks of 8 elements); kDecode issued
+          // these copies at entry and only waits for them here.
+          if constexpr (C::DEC) {
+            ptx::cp_async_wait_all();
+          } else {
+            const uint4* src = reinterpret_cast<const uint4*>(p.q + row_id * p.Dqk + d0);
+            for (int cq = half * (C::DH / 16); cq < (half + 1) * (C::DH / 16); ++cq) {
+              uint4 v = make_uint4(0, 0, 0, 0);
+              if (row_valid) v = src[cq];
+              const int dc = cq >> 3, cc = cq & 7;
+              const uint32_t addr = sQ + dc * 16384 + t * 128 + ((cc ^ (t & 7)) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x),
+                           "r"(v.y), "r"(v.z), "r"(v.w)
+                           : "memory");
+            }
           }
           ptx::fence_proxy_async_smem();
           asm volatile("bar.sync 1, 256;" ::: "memory");
@@ -1281,7 +1433,39 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
         return reinterpret_cast<float4*>(p.sk_o) +
                ((static_cast<long long>(sl) * 2 + rank) * 64 + c4) * 128 + t;
       };
-      if (pc.kind == 3) {
+      if (C::DEC && pc.kind == 3) {
+        // Cluster split: (max, sum) of every row into the idle query buffer and
+        // the fp32 O rows into the idle ring (every load has been consumed and
+        // every MMA has completed), for the cluster merge at the end.  Row t's
+        // 16-byte chunk c sits at chunk c ^ (t & 15) of its DV * 4-byte row.
+        if (count == 0) {
+          // The query copies issued at entry were never waited for: let every
+          // one of them land before the query buffer is reused.
+          ptx::cp_async_wait_all();
+          asm volatile("bar.sync 1, 256;" ::: "memory");
+        }
+        if (half == 0) reinterpret_cast<float2*>(smem + C::Q_OFF)[t] = make_float2(m_run, l);
+        if (count > 0) {
+#pragma unroll 1
+          for (int cch = 0; cch < C::DV / 64; ++cch) {
+            const int col = half * (C::DV / 2) + cch * 32;
+            uint32_t r[32];
+            ptx::tmem_ld32(lane_base + col, r);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence(r);
+            if (row_valid) {
+              const uint32_t rowa = sbase + C::RING_OFF + static_cast<uint32_t>(t * C::DV * 4);
+#pragma unroll
+              for (int g = 0; g < 8; ++g) {
+                const uint32_t ci = static_cast<uint32_t>((col >> 2) + g) ^ static_cast<uint32_t>(t & 15);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rowa + (ci << 4)),
+                             "r"(r[4 * g]), "r"(r[4 * g + 1]), "r"(r[4 * g + 2]), "r"(r[4 * g + 3])
+                             : "memory");
+              }
+            }
+          }
+        }
+      } else if (pc.kind == 3) {
         // Planned split: fp32 partials merged by the combine kernel.
         if (row_valid && half == 0 && (!PAIR || rank == 0)) {
           const long long pr = static_cast<long long>(w.split) * R + row_id;
@@ -1306,6 +1490,8 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
             }
           }
         }
+      } else if (C::DEC) {
+        // (decode pieces are always cluster splits)
       } else if (pc.kind == 2) {
         // Suffix piece: leave the unnormalised share for the unit that holds the
         // query tile's prefix, then publish it.
@@ -1456,6 +1642,91 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
         warp_arrive(kBarOFree);
       }
       g0 += count;
+    }
+    if constexpr (C::DEC) {
+      // Cluster merge.  Every CTA (split) of the cluster has left (max, sum)
+      // per row in its query buffer and its fp32 O rows in its ring.  CTA
+      // `crank` merges output columns [crank * DV / CS, (crank + 1) * DV / CS)
+      // of every row over the CS splits in rank order:
+      //   M = max_s m_s,  L = sum_s 2^(m_s - M) l_s,  O = sum_s 2^(m_s - M) O_s,
+      // skipping splits that saw no visible key (l_s == 0), and stores O / L
+      // (one cluster per group) or (M, L, O) as this cluster's partial for the
+      // combine kernel.  A row's result depends on that row's partials only.
+      // If any CTA of the cluster gave up a wait, the merged rows are NaN.  The
+      // producer / MMA warpgroup takes part in the two cluster barriers.
+      ptx::cp_async_wait_all();
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      ptx::cluster_sync();  // all partials and abort flags of the cluster are in place
+      const int CS = p.dec_cs;
+      const uint32_t crank = ptx::cluster_ctarank();
+      uint32_t aborted[kMaxDecodeClusterCtas];
+#pragma unroll
+      for (int r = 0; r < kMaxDecodeClusterCtas; ++r)
+        aborted[r] = r < CS ? ptx::ld_cluster_u32(ptx::mapa(sbase + C::BAR_OFF + 244, r)) : 0u;
+      bool bad = false;
+#pragma unroll
+      for (int r = 0; r < kMaxDecodeClusterCtas; ++r) bad |= aborted[r] != 0u;
+      const Work w = make_work<BN, QROWS>(p, item, 0);
+      const int ncol = C::DV / CS;
+      const int nch = ncol >> 2;
+      const int c0 = static_cast<int>(crank) * ncol;
+      const int base = p.Lk - p.Lq;
+      const long long R = static_cast<long long>(p.B) * p.Hq * p.Lq;
+      const int cl = w.split / CS;  // this cluster's index within its group
+      const float qnan = __int_as_float(0x7fc00000);
+      for (int idx = threadIdx.x; idx < 128 * nch; idx += 256) {
+        const int tt = idx / nch, ch = idx - tt * nch;
+        const int hl = tt >> 3;
+        const int i = ((((tt & 7) - base) % 8) + 8) % 8;
+        const int h = w.h0 + hl;
+        if (!(i < p.Lq && hl < min(p.G, 16) && h < (w.hkv + 1) * p.G)) continue;
+        const long long row_id = (static_cast<long long>(w.b) * p.Hq + h) * p.Lq + i;
+        const uint32_t mla = sbase + C::Q_OFF + static_cast<uint32_t>(tt * 8);
+        const uint32_t ci = static_cast<uint32_t>((c0 >> 2) + ch) ^ static_cast<uint32_t>(tt & 15);
+        const uint32_t oa = sbase + C::RING_OFF + static_cast<uint32_t>(tt * C::DV * 4) + (ci << 4);
+        // All loads first (issued back to back), then the arithmetic.
+        float2 ml[kMaxDecodeClusterCtas];
+        float4 o[kMaxDecodeClusterCtas];
+#pragma unroll
+        for (int r = 0; r < kMaxDecodeClusterCtas; ++r)
+          if (r < CS) ml[r] = ptx::ld_cluster_f2(ptx::mapa(mla, r));
+#pragma unroll
+        for (int r = 0; r < kMaxDecodeClusterCtas; ++r)
+          if (r < CS) o[r] = ptx::ld_cluster_f4(ptx::mapa(oa, r));
+        float M = -INFINITY;
+#pragma unroll
+        for (int r = 0; r < kMaxDecodeClusterCtas; ++r)
+          if (r < CS && ml[r].y > 0.f) M = fmaxf(M, ml[r].x);
+        float L = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < kMaxDecodeClusterCtas; ++r) {
+          if (r < CS && ml[r].y > 0.f) {
+            const float wgt = ptx::ex2(ml[r].x - M);
+            L = fmaf(wgt, ml[r].y, L);
+            acc.x = fmaf(wgt, o[r].x, acc.x);
+            acc.y = fmaf(wgt, o[r].y, acc.y);
+            acc.z = fmaf(wgt, o[r].z, acc.z);
+            acc.w = fmaf(wgt, o[r].w, acc.w);
+          }
+        }
+        const int col = c0 + 4 * ch;
+        if (p.dec_nc == 1) {
+          const float inv = bad ? qnan : (L > 0.f ? 1.f / L : 0.f);
+          uint2 v;
+          v.x = pack2(acc.x * inv, acc.y * inv, BF16);
+          v.y = pack2(acc.z * inv, acc.w * inv, BF16);
+          *reinterpret_cast<uint2*>(p.out + row_id * p.D + col) = v;
+        } else {
+          if (bad) acc = make_float4(qnan, qnan, qnan, qnan);
+          const long long pr = static_cast<long long>(cl) * R + row_id;
+          *reinterpret_cast<float4*>(p.part_o + pr * p.D + col) = acc;
+          if (crank == 0 && ch == 0)
+            reinterpret_cast<float2*>(p.part_ml)[pr] = make_float2(M, bad ? qnan : L);
+        }
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");  // (re)converge before the aligned barrier
+      ptx::cluster_sync();  // no CTA reads another's shared memory after this
     }
   }
 

@@ -126,25 +126,30 @@ int sdpa_prefill_launches(int B, int Hq, int Hkv, int Lq, int Lk, int D, int cau
 /*
  * Decode / speculative verify: 1 <= Lq <= 8 query rows per head over Lk keys.
  *
- * Same arguments and semantics as sdpa_prefill; the workspace is required
- * (at least sdpa_decode_workspace_bytes(B, Hq, Hkv, Lq, D) bytes; the size
- * does not depend on Lk).
+ * Same arguments and semantics as sdpa_prefill.  The workspace must hold at
+ * least sdpa_decode_workspace_bytes(B, Hq, Hkv, Lq, D) bytes; when that is 0
+ * (head dims up to 256 whenever one cluster of splits covers each head group)
+ * the workspace may be NULL.  The size does not depend on Lk.
  *
  * Row invariance ("fix: Gemma 4 MTP never engages on CUDA (GB10)", sections
  * "Proposed Solution" and "Acceptance Criteria"): row i of a call with Lq = M
  * is bit-identical to the Lq = 1 call with the same B, Hq, Hkv, D, dtype,
- * scale, causal, window and workspace size whose key/value prefix is trimmed
- * to Lk - M + 1 + i keys.  The key range is cut into 128-key tiles at fixed
+ * scale, causal and window whose key/value prefix is trimmed to
+ * Lk - M + 1 + i keys.  The key range is cut into 64-key tiles at fixed
  * absolute positions, dealt round-robin over a split count that depends only
- * on (B, Hkv, Hq/Hkv, D) and the device's SM count, and merged in a fixed
- * order; a row's arithmetic never depends on the other rows of the call.
+ * on (B, Hkv, Hq/Hkv, D, window) and the device, and the splits' partials are
+ * merged in a fixed order (head dims up to 256: inside one launch, by the
+ * thread-block cluster the splits of a head group form; head dim 512: by a
+ * second kernel); a row's arithmetic never depends on the other rows of the
+ * call.
  */
 int sdpa_decode(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
                 int Lq, int Lk, int D, float scale, int causal, int window, int dtype,
                 void* workspace, size_t workspace_bytes, sdpa_stream_t stream);
 
-/* Workspace bytes sdpa_decode needs on the current device (0 on bad arguments);
- * enough for any window (a windowed call splits its keys into fewer pieces). */
+/* Workspace bytes sdpa_decode needs on the current device (0 on bad arguments,
+ * or when the call needs none).  It is computed without a window and is an
+ * upper bound for every window: a windowed call needs at most this much. */
 size_t sdpa_decode_workspace_bytes(int B, int Hq, int Hkv, int Lq, int D);
 
 /*
@@ -216,7 +221,9 @@ int sdpa_decode_ex(const void* q, const void* k, const void* v, void* out, int B
  * current device and clears the status word.  *detail (if not NULL) receives
  * the raw device code (0 if none): 0x100..0x10a identify the pipeline wait that
  * gave up, 0x10b a shared-memory window that was not 1024-byte aligned, 0x10c a
- * 2-CTA kernel that found itself outside a cluster of two.  In every case the
+ * 2-CTA kernel that found itself outside a cluster of two (or a decode kernel
+ * in a cluster of another size than planned), 0x10d a decode CTA beyond the
+ * planned grid.  In every case the
  * kernel stopped without touching memory it should not and its output is
  * unspecified. */
 int sdpa_device_status(sdpa_stream_t stream, int* detail);
@@ -276,7 +283,9 @@ int sdpa_selftest_timeout(const void* q, const void* k, const void* v, void* out
  *    call before any stream capture on that device.
  *  - A call whose split partials need more than SDPA_NOALLOC_SCRATCH_BYTES is
  *    rejected with SDPA_ERR_SCRATCH_LIMIT before anything is queued; the need
- *    is what sdpa_decode_workspace_bytes(B, Hq, Hkv, Lq, D) reports.
+ *    is at most what sdpa_decode_workspace_bytes(B, Hq, Hkv, Lq, D) reports
+ *    (a windowed call may need less, and calls whose head groups are each
+ *    covered by one cluster of splits need none).
  *  - Every call on a device shares the one array, and the array keeps the
  *    previous call's contents.  Nothing in it has to start at zero: each call
  *    writes every partial it later reads.  Two calls whose work overlaps on
