@@ -194,3 +194,27 @@ def test_large_scale_exercises_the_rescale(D):
     assert gb.device_status()[0] == 0
     ref = oracle.sdpa(q, k, v, causal=True, scale=1.0)
     assert max_err(out, ref) < 4e-3
+
+
+def test_decode_workspace_rules():
+    """Head dims up to 256 with one cluster of splits per head group need no
+    workspace (NULL is accepted and the result matches the oracle); head dim
+    512 merges split partials in a second kernel and refuses a NULL workspace."""
+    lib = gb.load_library()
+    stream = torch.cuda.current_stream().cuda_stream
+    for D, need_ws in ((256, False), (512, True)):
+        Hq, Hkv, Lq, Lk = 16, 8 if D == 256 else 1, 4, 5000
+        q, k, v = draw(1, Hq, Hkv, Lq, Lk, D, torch.float16, seed=D)
+        assert (gb.decode_workspace_bytes(1, Hq, Hkv, Lq, D) > 0) == need_ws
+        qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+        out = torch.zeros_like(qd)
+        rc = lib.sdpa_decode(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), out.data_ptr(), 1, Hq,
+                             Hkv, Lq, Lk, D, 1.0 / math.sqrt(D), 1, 1024, 0, None, 0, stream)
+        if need_ws:
+            assert rc == -3
+            continue
+        assert rc == 0
+        torch.cuda.synchronize()
+        assert gb.device_status()[0] == 0
+        ref = oracle.sdpa(q, k, v, causal=True, window=1024)
+        assert max_err(out, ref) < 4e-3
