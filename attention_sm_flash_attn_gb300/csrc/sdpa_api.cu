@@ -198,7 +198,23 @@ int launch_mode(int mode, int D, int Dv, int window, bool bias) {
 }
 
 bool two_sm(int mode) { return mode == gbsdpa::kDuo || mode == gbsdpa::kDuoQ; }
-int qtile_rows(int mode) { return two_sm(mode) ? 256 : 128; }
+// Query-tile geometry of a prefill call: rows per tile and query heads per work
+// item.  A 2-SM pair takes 128 rows of two query heads of one kv head when the
+// group size is even (both CTAs then see the same key band: a sliding window
+// spans window + 127 keys instead of window + 255), else 256 rows of one head.
+struct QTiling {
+  int rows = 128, heads = 1;
+};
+QTiling qtiling(int mode, int G) {
+  QTiling t;
+  if (two_sm(mode)) {
+    if (G % 2 == 0)
+      t.heads = 2;
+    else
+      t.rows = 256;
+  }
+  return t;
+}
 int key_tile(int mode) { return (mode == gbsdpa::kPair || mode == gbsdpa::kDecode) ? 64 : 128; }
 
 // Key tiles the longest query tile (of `rows` rows) visits.
@@ -214,10 +230,12 @@ long long max_tiles_per_qtile(int Lq, int Lk, int causal, int window, int bn, in
 // How many contiguous shares to cut each query tile's key range into.  A
 // simple wave model: time ~ ceil(ctas / sms) * ceil(tiles / s), plus the cost
 // of writing and re-reading the fp32 partials.
-int plan_prefill_splits(int sms, int B, int Hq, int Lq, int Lk, int D, int causal, int window) {
+int plan_prefill_splits(int sms, int B, int Hq, int Hkv, int Lq, int Lk, int D, int causal,
+                        int window) {
   const int mode = choose_mode(false, D, causal ? window : 0);
-  const int bn = key_tile(mode), rows = qtile_rows(mode);
-  const long long items = static_cast<long long>(B) * Hq * ((Lq + rows - 1) / rows);
+  const QTiling qt = qtiling(mode, Hq / Hkv);
+  const int bn = key_tile(mode), rows = qt.rows;
+  const long long items = static_cast<long long>(B) * (Hq / qt.heads) * ((Lq + rows - 1) / rows);
   const long long per_cta = mode == gbsdpa::kSingle ? 1 : 2;
   const long long slots = std::max<long long>(1, sms / per_cta);
   const long long T = max_tiles_per_qtile(Lq, Lk, causal, window, bn, rows);
@@ -323,10 +341,12 @@ long long qtile_key_tiles(int q0, int rows, int Lq, int Lk, int causal, int wind
   return (hi + bn - 1) / bn - lo / bn;
 }
 
-long long total_key_tiles(int B, int Hq, int Lq, int Lk, int causal, int window, int bn, int rows) {
+// Key tiles of all work items (each item: one query tile of `heads` heads).
+long long total_key_tiles(int B, int Hq, int Lq, int Lk, int causal, int window, int bn, int rows,
+                          int heads) {
   long long w = 0;
   for (int q0 = 0; q0 < Lq; q0 += rows) w += qtile_key_tiles(q0, rows, Lq, Lk, causal, window, bn);
-  return w * B * Hq;
+  return w * B * (Hq / heads);
 }
 
 // Workspace of a persistent launch: per (slot, rank) 128 x 256 fp32 partial
@@ -358,11 +378,11 @@ struct TailPlan {
 };
 
 TailPlan plan_tail(long long units, int B, int Hq, int Lq, int Lk, int causal, int window, int bn,
-                   int rows) {
+                   int rows, int heads) {
   constexpr long long kPieceCost = 3, kMergeCost = 3;
   TailPlan t;
   const long long n_qtiles = (Lq + rows - 1) / rows;
-  const long long n_per = static_cast<long long>(B) * Hq;
+  const long long n_per = static_cast<long long>(B) * (Hq / heads);
   const long long N = n_qtiles * n_per, U = units;
   const long long r = N % U, base = N - r;
   if (r == 0) return t;
@@ -398,15 +418,16 @@ TailPlan plan_tail(long long units, int B, int Hq, int Lq, int Lk, int causal, i
 
 // Units for a persistent prefill launch (0: one CTA per query tile instead).
 template <bool BF16>
-long long persistent_units(DeviceState* st, int mode, int D, int B, int Hq, int Lq, int Lk,
-                           int causal, int window, int Dv = 0, bool bias = false) {
+long long persistent_units(DeviceState* st, int mode, int D, int B, int Hq, int Hkv, int Lq,
+                           int Lk, int causal, int window, int Dv = 0, bool bias = false) {
   if (Dv <= 0) Dv = D;
   const int lm = launch_mode(mode, D, Dv, causal ? window : 0, bias);
   const int units = bias ? gbsdpa_host::resident_bias_variant(BF16, lm, D, Dv, st)
                          : gbsdpa_host::resident_variant<BF16, false>(lm, D, Dv, st);
   if (units <= 0) return 0;
+  const QTiling qt = qtiling(mode, Hq / Hkv);
   const long long W =
-      total_key_tiles(B, Hq, Lq, Lk, causal, window, key_tile(mode), qtile_rows(mode));
+      total_key_tiles(B, Hq, Lq, Lk, causal, window, key_tile(mode), qt.rows, qt.heads);
   return std::min<long long>(units, W);
 }
 
@@ -483,7 +504,9 @@ int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, i
     p.bias_sq = bias.sq;
     p.bias_vec = aligned16(bias.ptr) && bias.sb % 8 == 0 && bias.sh % 8 == 0 && bias.sq % 8 == 0;
   }
-  p.n_qtiles = (Lq + qtile_rows(mode) - 1) / qtile_rows(mode);
+  const QTiling qt = qtiling(mode, Hq / Hkv);
+  p.hpair = qt.heads == 2 ? 1 : 0;
+  p.n_qtiles = (Lq + qt.rows - 1) / qt.rows;
   p.n_splits = n_splits;
   p.n_hb = (p.G + 15) / 16;
   p.write_partial = write_partial ? 1 : 0;
@@ -495,7 +518,7 @@ int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, i
     p.persistent = 1;
     p.n_units = static_cast<int>(sk_units);
     const TailPlan tp = plan_tail(sk_units, B, Hq, Lq, Lk, causal, window, key_tile(mode),
-                                  qtile_rows(mode));
+                                  qt.rows, qt.heads);
     p.tail_L = tp.L;
     p.tail_SS = tp.SS;
     p.tail_US = tp.US;
@@ -510,7 +533,7 @@ int run(const void* q, const void* k, const void* v, void* out, int B, int Hq, i
   } else if (decode)
     items = static_cast<long long>(B) * Hkv * n_splits * p.n_hb;
   else
-    items = static_cast<long long>(B) * Hq * p.n_qtiles * n_splits;
+    items = static_cast<long long>(B) * (Hq / qt.heads) * p.n_qtiles * n_splits;
   const int lm = launch_mode(mode, D, Dv, window, p.bias != nullptr);
   rc = p.bias ? gbsdpa_host::launch_bias_variant(BF16, lm, D, Dv, p, items, stream, st)
               : gbsdpa_host::launch_variant<BF16, false>(lm, D, Dv, p, items, stream, st);
@@ -533,10 +556,11 @@ size_t sdpa_prefill_workspace_bytes(int B, int Hq, int Hkv, int Lq, int Lk, int 
   if (window < 0 || (causal && Lq > Lk)) return 0;
   if (device_state(&st)) return 0;
   const int mode = choose_mode(false, D, causal ? window : 0);
-  const long long u = std::max(persistent_units<false>(st, mode, D, B, Hq, Lq, Lk, causal, window),
-                               persistent_units<true>(st, mode, D, B, Hq, Lq, Lk, causal, window));
+  const long long u =
+      std::max(persistent_units<false>(st, mode, D, B, Hq, Hkv, Lq, Lk, causal, window),
+               persistent_units<true>(st, mode, D, B, Hq, Hkv, Lq, Lk, causal, window));
   if (u > 0) return sk_layout(u).bytes;
-  const int s = plan_prefill_splits(st->sms, B, Hq, Lq, Lk, D, causal, window);
+  const int s = plan_prefill_splits(st->sms, B, Hq, Hkv, Lq, Lk, D, causal, window);
   if (s <= 1) return 0;
   return partial_bytes(static_cast<long long>(B) * Hq * Lq, D, s);
 }
@@ -552,9 +576,9 @@ int sdpa_prefill_launches(int B, int Hq, int Hkv, int Lq, int Lk, int D, int cau
   int rc = device_state(&st);
   if (rc) return rc;
   const int mode = choose_mode(false, D, window);
-  const long long u = persistent_units<false>(st, mode, D, B, Hq, Lq, Lk, causal, window);
+  const long long u = persistent_units<false>(st, mode, D, B, Hq, Hkv, Lq, Lk, causal, window);
   if (u > 0) return 1;  // persistent with the workspace, one CTA per tile without
-  const int s = plan_prefill_splits(st->sms, B, Hq, Lq, Lk, D, causal, window);
+  const int s = plan_prefill_splits(st->sms, B, Hq, Hkv, Lq, Lk, D, causal, window);
   return (s > 1 && workspace_bytes >= partial_bytes(static_cast<long long>(B) * Hq * Lq, D, s))
              ? 2 : 1;
 }
@@ -592,14 +616,16 @@ static int prefill_impl(const void* q, const void* k, const void* v, void* out, 
   const int mode = choose_mode(false, D, window);
   const bool has_bias = bias.ptr != nullptr;
   const long long u =
-      bf16 ? persistent_units<true>(st, mode, D, B, Hq, Lq, Lk, causal, window, Dv, has_bias)
-           : persistent_units<false>(st, mode, D, B, Hq, Lq, Lk, causal, window, Dv, has_bias);
+      bf16 ? persistent_units<true>(st, mode, D, B, Hq, Hkv, Lq, Lk, causal, window, Dv,
+                                    has_bias)
+           : persistent_units<false>(st, mode, D, B, Hq, Hkv, Lq, Lk, causal, window, Dv,
+                                     has_bias);
   if (u > 0 && workspace && workspace_bytes >= sk_layout(u).bytes)
     return bf16 ? run<true>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, false, 1,
                             false, workspace, strm, st, 0, u, kv_cap, kv_ring, Dv, bias)
                 : run<false>(q, k, v, out, B, Hq, Hkv, Lq, Lk, D, scale, causal, window, false, 1,
                              false, workspace, strm, st, 0, u, kv_cap, kv_ring, Dv, bias);
-  int s = u > 0 ? 1 : plan_prefill_splits(st->sms, B, Hq, Lq, Lk, D, causal, window);
+  int s = u > 0 ? 1 : plan_prefill_splits(st->sms, B, Hq, Hkv, Lq, Lk, D, causal, window);
   if (s > 1 && (!workspace ||
                 workspace_bytes < partial_bytes(static_cast<long long>(B) * Hq * Lq, Dv, s)))
     s = 1;
@@ -732,9 +758,10 @@ int sdpa_selftest_timeout(const void* q, const void* k, const void* v, void* out
     rc = device_state(&st);
     if (rc) return rc;
     const int mode = choose_mode(false, D, 0);
-    const long long u = persistent_units<false>(st, mode, D, B, Hq, Lq, Lk, 1, 0);
+    const long long u = persistent_units<false>(st, mode, D, B, Hq, Hkv, Lq, Lk, 1, 0);
     if (u <= 0) return SDPA_ERR_UNSUPPORTED;
-    if (plan_tail(u, B, Hq, Lq, Lk, 1, 0, key_tile(mode), qtile_rows(mode)).US <= 0)
+    const QTiling qt = qtiling(mode, Hq / Hkv);
+    if (plan_tail(u, B, Hq, Lq, Lk, 1, 0, key_tile(mode), qt.rows, qt.heads).US <= 0)
       return SDPA_ERR_UNSUPPORTED;  // no suffix pieces on this device: nothing to withhold
     if (!workspace || workspace_bytes < sk_layout(u).bytes || !aligned16(workspace))
       return SDPA_ERR_WORKSPACE;

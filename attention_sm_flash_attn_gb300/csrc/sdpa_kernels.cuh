@@ -84,7 +84,11 @@ struct AttnParams {
   int causal, window;
   float c;        // scale * log2(e)
   int decode;     // 0 = prefill, 1 = decode
-  int n_qtiles;   // prefill: ceil(Lq / 128)
+  int n_qtiles;   // prefill: query tiles per head (ceil(Lq / rows of a tile))
+  // 2-SM variants: 1 = a CTA pair owns 128 query rows of two query heads of one
+  // kv head (CTA `rank` takes head 2 * pair + rank), 0 = 256 consecutive rows
+  // of one head (CTA `rank` takes rows 128 * rank ..).
+  int hpair;
   int n_splits;   // prefill: 1 => final output written directly; decode: fixed split count
   int n_hb;       // decode: query-head blocks of 16 per kv head
   // kDecode: the n_splits splits of a (batch, kv head, head block) group are
@@ -282,17 +286,31 @@ struct Work {
   int t_begin, t_step, t_count;
 };
 
-// Work of one CTA.  Prefill items walk (query head within its group, split, kv
-// head, batch, query tile) with the longest causal query tiles first; a query
-// tile has QROWS rows (256 for a 2-SM pair, of which CTA `rank` owns 128).
-// Decode items walk (head block, split, kv head, batch).
+// Query heads per prefill item and query rows per tile.  A 2-SM pair (QROWS
+// 256) owns either 256 consecutive rows of one head or, with p.hpair, 128 rows
+// of two heads of the same kv head; one CTA owns 128 rows of one head.
+template <int QROWS>
+__device__ __forceinline__ int item_heads(const AttnParams& p) {
+  return (QROWS == 256 && p.hpair) ? 2 : 1;
+}
+template <int QROWS>
+__device__ __forceinline__ int tile_rows(const AttnParams& p) {
+  return (QROWS == 256 && !p.hpair) ? 256 : 128;
+}
+
+// Work of one CTA.  Prefill items walk (query heads within their group, split,
+// kv head, batch, query tile) with the longest causal query tiles first; see
+// item_heads / tile_rows for what an item of a 2-SM pair covers.  Decode items
+// walk (head block, split, kv head, batch).
 template <int BN, int QROWS>
 __device__ __forceinline__ Work make_work(const AttnParams& p, int item, int rank) {
   Work w;
   int lo, hi;
   if (!p.decode) {
-    const int hl = item % p.G;
-    item /= p.G;
+    const int ih = item_heads<QROWS>(p), rows = tile_rows<QROWS>(p);
+    const int ng = p.G / ih;
+    const int hq = item % ng;
+    item /= ng;
     w.split = item % p.n_splits;
     item /= p.n_splits;
     w.hkv = item % p.Hkv;
@@ -300,10 +318,10 @@ __device__ __forceinline__ Work make_work(const AttnParams& p, int item, int ran
     w.b = item % p.B;
     item /= p.B;
     const int qt = p.n_qtiles - 1 - item;  // longest causal tiles first
-    w.h0 = w.hkv * p.G + hl;
-    const int q0 = qt * QROWS;
-    w.m0 = q0 + (QROWS == 256 ? rank * 128 : 0);
-    const int qlast = min(q0 + QROWS, p.Lq) - 1;
+    w.h0 = w.hkv * p.G + hq * ih + (ih == 2 ? rank : 0);
+    const int q0 = qt * rows;
+    w.m0 = q0 + (rows == 256 ? rank * 128 : 0);
+    const int qlast = min(q0 + rows, p.Lq) - 1;
     w.pmin = p.Lk - p.Lq + q0;
     w.pmax = p.Lk - p.Lq + qlast;
     lo = (p.causal && p.window) ? max(0, w.pmin - p.window + 1) : 0;
@@ -361,8 +379,9 @@ __device__ __forceinline__ Work make_work(const AttnParams& p, int item, int ran
 // Key tiles of a query tile (the same count make_work visits).
 template <int BN, int QROWS>
 __device__ __forceinline__ int item_tiles_for_qt(const AttnParams& p, int qt) {
-  const int q0 = qt * QROWS;
-  const int qlast = min(q0 + QROWS, p.Lq) - 1;
+  const int rows = tile_rows<QROWS>(p);
+  const int q0 = qt * rows;
+  const int qlast = min(q0 + rows, p.Lq) - 1;
   const int pmin = p.Lk - p.Lq + q0, pmax = p.Lk - p.Lq + qlast;
   const int lo = (p.causal && p.window) ? max(0, pmin - p.window + 1) : 0;
   const int hi = p.causal ? min(p.Lk, pmax + 1) : p.Lk;
@@ -371,7 +390,8 @@ __device__ __forceinline__ int item_tiles_for_qt(const AttnParams& p, int qt) {
 
 template <int BN, int QROWS>
 __device__ __forceinline__ int item_tiles(const AttnParams& p, int idx) {
-  return item_tiles_for_qt<BN, QROWS>(p, p.n_qtiles - 1 - idx / (p.G * p.Hkv * p.B));
+  return item_tiles_for_qt<BN, QROWS>(p, p.n_qtiles - 1 -
+                                            idx / (p.G / item_heads<QROWS>(p) * p.Hkv * p.B));
 }
 
 // Work of item `idx`, key tiles [t0, t0 + cnt) of its visible range.
@@ -380,18 +400,20 @@ __device__ __forceinline__ Work item_work(const AttnParams& p, int idx, int rank
                                           int cnt) {
   Work w;
   int item = idx;
-  const int hl = item % p.G;
-  item /= p.G;
+  const int ih = item_heads<QROWS>(p), rows = tile_rows<QROWS>(p);
+  const int ng = p.G / ih;
+  const int hq = item % ng;
+  item /= ng;
   w.split = 0;
   w.hkv = item % p.Hkv;
   item /= p.Hkv;
   w.b = item % p.B;
   item /= p.B;
   const int qt = p.n_qtiles - 1 - item;
-  w.h0 = w.hkv * p.G + hl;
-  const int q0 = qt * QROWS;
-  w.m0 = q0 + (QROWS == 256 ? rank * 128 : 0);
-  const int qlast = min(q0 + QROWS, p.Lq) - 1;
+  w.h0 = w.hkv * p.G + hq * ih + (ih == 2 ? rank : 0);
+  const int q0 = qt * rows;
+  w.m0 = q0 + (rows == 256 ? rank * 128 : 0);
+  const int qlast = min(q0 + rows, p.Lq) - 1;
   w.pmin = p.Lk - p.Lq + q0;
   w.pmax = p.Lk - p.Lq + qlast;
   const int lo = (p.causal && p.window) ? max(0, w.pmin - p.window + 1) : 0;
@@ -437,7 +459,7 @@ __device__ __forceinline__ void iter_init(const AttnParams& p, IterState& st, in
     st.stage = 4;
     return;
   }
-  const int N = p.n_qtiles * p.G * p.Hkv * p.B;
+  const int N = p.n_qtiles * (p.G / item_heads<QROWS>(p)) * p.Hkv * p.B;
   const int U = p.n_units;
   st.n_full = N / U;
   st.r = N - st.n_full * U;
