@@ -188,13 +188,14 @@ int choose_mode(bool decode, int D, int window) {
 }
 
 
-// The instantiation a call of this shape launches: at head dim 256 with no
-// window and no bias the 2-SM variant keeps Q in tensor memory (measured
-// faster over long key ranges; a window's short pieces and a bias's loads do
-// better with the form that keeps P in tensor memory).
+// The instantiation a call of this shape launches: at head dim 256 without a
+// bias the 2-SM variant keeps Q in tensor memory (measured faster over long
+// key ranges, and, with head-paired tiles, over a sliding window's short
+// pieces; a bias's loads do better with the form that keeps P in tensor
+// memory).
 int launch_mode(int mode, int D, int Dv, int window, bool bias) {
-  return (mode == gbsdpa::kDuo && D == 256 && Dv == 256 && window == 0 && !bias) ? gbsdpa::kDuoQ
-                                                                                 : mode;
+  (void)window;
+  return (mode == gbsdpa::kDuo && D == 256 && Dv == 256 && !bias) ? gbsdpa::kDuoQ : mode;
 }
 
 bool two_sm(int mode) { return mode == gbsdpa::kDuo || mode == gbsdpa::kDuoQ; }

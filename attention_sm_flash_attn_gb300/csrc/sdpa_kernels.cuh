@@ -51,6 +51,9 @@
 
 namespace gbsdpa {
 
+// Barrier that signals "S buffer `buf` holds a finished Q.K^T product".
+__host__ __device__ constexpr int sfull_bar(int buf) { return buf < 2 ? 17 + buf : 27; }
+
 // Device status codes (bit pattern identifies the wait that gave up).
 enum : int {
   kDevOk = 0,
@@ -201,7 +204,13 @@ struct Cfg {
   static constexpr int ITER_OFF = RED_OFF + 2048;
   static constexpr int SMEM_BYTES = ITER_OFF + 768;
   static constexpr int S_COL = 256;  // TMEM: O in columns [0,256), S buffers after it
-  static constexpr int NSBUF = QTM ? 1 : 2;          // S buffers
+  // S buffers: kDuoQ has one (released by its own barrier), the head-dim-split
+  // pair three (so the MMA can run two tiles ahead while the softmax swaps
+  // partial scores with the peer), the others two.
+  static constexpr int NSBUF = QTM ? 1 : (PAIR ? 3 : 2);
+  // Q.K^T products the MMA issuer keeps ahead of P.V (every S buffer but the
+  // one P.V reads).
+  static constexpr int S_AHEAD = NSBUF == 3 ? 2 : 1;
   static constexpr int Q_COL = S_COL + NSBUF * BN;   // Q (QTM): DH/2 columns
   // warps 0-7 softmax (warpgroups 0, 1), 8 producer, 9 MMA, 10-11 idle (warpgroup 2)
   static constexpr int NTHREADS = 384;
@@ -246,9 +255,12 @@ enum {
   kBarXFree = 24,
   kBarDrain = 25,
   kBarSFree = 26,    // Q in TMEM: the softmax has read the (single) S buffer
-  kNumBars = 27,
+  kBarSFull2 = 27,   // third S buffer (head-dim-split pair)
+  kNumBars = 28,
 };
 static_assert(kNumBars * 8 <= 240, "barriers end below the TMEM slot and abort flag");
+static_assert(sfull_bar(0) == kBarSFull && sfull_bar(1) == kBarSFull + 1 && sfull_bar(2) == kBarSFull2,
+              "S-full barriers");
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 
@@ -683,7 +695,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
       ptx::mbar_init(bar(kBarKvFull + s), 1);
       ptx::mbar_init(bar(kBarKvEmpty + s), 1);
     }
-    for (int b = 0; b < 2; ++b) ptx::mbar_init(bar(kBarSFull + b), 1);
+    for (int b = 0; b < 3; ++b) ptx::mbar_init(bar(sfull_bar(b)), 1);
     ptx::mbar_init(bar(kBarPFull), C::kPFullArrivals);
     ptx::mbar_init(bar(kBarPvDone), 1);
     ptx::mbar_init(bar(kBarQFree), 1);
@@ -886,12 +898,12 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
             ring_issued = n + 1;
           }
         };
-        load_k(0);
-        for (int j = 1; j < count && ok; ++j) {
-          load_k(j);
-          load_v(j - 1);
+        // The MMA issuer consumes the ring in this order: K of tile j comes
+        // S_AHEAD tiles before V of tile j - S_AHEAD.
+        for (int j = 0; j < count + C::S_AHEAD && ok; ++j) {
+          if (j < count) load_k(j);
+          if (ok && j >= C::S_AHEAD) load_v(j - C::S_AHEAD);
         }
-        if (ok) load_v(count - 1);
       }
     }
   } else if (warp == C::kMmaWarp) {
@@ -941,7 +953,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
             ptx::tc_fence_after();
           }
         }
-        const uint32_t d_tmem = tmem + C::S_COL + (C::QTM ? 0 : (gt & 1) * BN);
+        const uint32_t d_tmem = tmem + C::S_COL + (static_cast<uint32_t>(gt) % C::NSBUF) * BN;
         for (int ks = 0; ks < C::KSUB; ++ks) {
           uint32_t sk;
           if (!consume(sk)) {
@@ -972,7 +984,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
           release();
           ++mma_issued;
         }
-        commit(kBarSFull + (C::QTM ? 0 : (gt & 1)));
+        commit(sfull_bar(static_cast<int>(static_cast<uint32_t>(gt) % C::NSBUF)));
       };
       auto do_pv = [&](int gt, int j) {  // j: tile index within the piece
         if (!wait_bar<DUO>(bar(kBarPFull), gt & 1, abort_flag, p.status, kDevTimeoutPFull)) {
@@ -1006,7 +1018,8 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
               mma(tmem, a, b, C::IDESC_PV, (j | vs | kk) != 0);
             } else {
               // A = P_gt in tensor memory (keys key..key+15 at columns key / 2).
-              const uint32_t a = tmem + C::S_COL + (gt & 1) * BN + key / 2;
+              const uint32_t a =
+                  tmem + C::S_COL + (static_cast<uint32_t>(gt) % C::NSBUF) * BN + key / 2;
               if constexpr (DUO)
                 ptx::mma_f16_ts_pair(tmem, a, b, C::IDESC_PV, (j | vs | kk) != 0);
               else
@@ -1045,14 +1058,31 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
             }
           commit(kBarQFree);
         }
-        do_s(g0);
-        if (!C::QTM && ok && count == 1) commit(kBarQFree);
-        for (int j = 1; j < count && ok; ++j) {
-          do_s(g0 + j);
-          if (!C::QTM && ok && j == count - 1) commit(kBarQFree);
-          if (ok) do_pv(g0 + j - 1, j - 1);
+        // S_j is issued S_AHEAD products ahead of P_{j-S_AHEAD}.V; its buffer last
+        // held S / P of tile j - NSBUF, whose P.V was issued before it (one
+        // thread's MMAs run in issue order).
+        if constexpr (C::S_AHEAD == 1) {
+          do_s(g0);
+          if (!C::QTM && ok && count == 1) commit(kBarQFree);
+          for (int j = 1; j < count && ok; ++j) {
+            do_s(g0 + j);
+            if (!C::QTM && ok && j == count - 1) commit(kBarQFree);
+            if (ok) do_pv(g0 + j - 1, j - 1);
+          }
+          if (ok) do_pv(g0 + count - 1, count - 1);
+        } else {
+          const int pro = min(count, C::S_AHEAD);
+          for (int j = 0; j < pro && ok; ++j) {
+            do_s(g0 + j);
+            if (ok && j == count - 1) commit(kBarQFree);
+          }
+          for (int j = C::S_AHEAD; j < count && ok; ++j) {
+            do_s(g0 + j);
+            if (ok && j == count - 1) commit(kBarQFree);
+            if (ok) do_pv(g0 + j - C::S_AHEAD, j - C::S_AHEAD);
+          }
+          for (int j = count - pro; j < count && ok; ++j) do_pv(g0 + j, j);
         }
-        if (ok) do_pv(g0 + count - 1, count - 1);
         g0 += count;
         ++done_pieces;
       }
@@ -1195,11 +1225,102 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
 
       float m_run = -INFINITY;  // running max of c * s (lazy: the true max may exceed it by < 8)
       float l = 0.f;            // this half's share of the row sum
+
+      // Pair: this CTA's partial scores of a tile go to the peer one tile ahead
+      // of the softmax that needs them.  send(gx) waits for S_gx, loads this
+      // CTA's partial (kept in registers for the add), stages the exchanged
+      // rows' HB columns (up to 4 KB a warp) in XS and one lane bulk-copies the
+      // block into the peer's X, completing the bytes on the peer's XFull
+      // barrier (thread 0 posts the expected byte count of the peer's block on
+      // ours).  recv(gx) waits for the peer's block, adds it and hands X back.
+      // Tile j's softmax runs while tile j + 1's blocks are in flight.
+      const uint32_t wofs = static_cast<uint32_t>(warp) * (32 * HB * 4);
+      const uint32_t rofs = wofs + xidx * (HB * 4);
+      const uint32_t xsw = xidx & (HB / 4 - 1);  // chunk swizzle of this row
+      auto load_partial = [&](int gx, float (&so)[HB]) {
+        const int bx = static_cast<int>(static_cast<uint32_t>(gx) % C::NSBUF);
+        if (alive)
+          alive = __all_sync(0xffffffffu,
+                             wait_bar(bar(sfull_bar(bx)), (static_cast<uint32_t>(gx) / C::NSBUF) & 1,
+                                      abort_flag, p.status, kDevTimeoutSFull));
+        if (alive) {
+          ptx::tc_fence_after();
+          uint32_t r[32];
+          ptx::tmem_ld32(lane_base + C::S_COL + bx * BN + half * HB, r);
+          ptx::tmem_wait_ld();
+          ptx::reg_fence(r);
+#pragma unroll
+          for (int e = 0; e < HB; ++e) so[e] = __uint_as_float(r[e]);
+        }
+      };
+      auto pair_send = [&](int gx, const float (&so)[HB]) {
+        // Exactly one arrival per phase of XFull: once a wait of this warp has
+        // given up, no further phase is waited for, and none is posted (a
+        // second arrival on a phase whose arrival is in would drive its
+        // pending count below zero).
+        if (threadIdx.x == 0 && alive) ptx::mbar_arrive_expect_tx(bar(kBarXFull), xbytes);
+        if (alive)  // the peer has read our previous block (and so it has landed)
+          alive = __all_sync(0xffffffffu, wait_bar<true>(bar(kBarXFree), (gx & 1) ^ 1, abort_flag,
+                                                         p.status, kDevTimeoutXFree));
+        if (alive) {
+          if (xrow) {
+#pragma unroll
+            for (int g = 0; g < HB / 4; ++g) {
+              const uint32_t off = rofs + ((g ^ xsw) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + C::XS_OFF + off),
+                           "r"(__float_as_uint(so[4 * g])), "r"(__float_as_uint(so[4 * g + 1])),
+                           "r"(__float_as_uint(so[4 * g + 2])), "r"(__float_as_uint(so[4 * g + 3]))
+                           : "memory");
+            }
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          const uint32_t nrows = __popc(xmask);
+          if (lane == 0 && nrows > 0)
+            ptx::bulk_copy_to_peer(ptx::mapa(sX + wofs, peer), sbase + C::XS_OFF + wofs,
+                                   nrows * HB * 4, ptx::mapa(bar(kBarXFull), peer));
+        }
+      };
+      auto pair_recv = [&](int gx, float (&si)[HB]) {
+        if (alive)
+          alive = __all_sync(0xffffffffu, wait_bar<true>(bar(kBarXFull), gx & 1, abort_flag,
+                                                         p.status, kDevTimeoutXFull));
+        if (alive && xrow) {
+#pragma unroll
+          for (int g = 0; g < HB / 4; ++g) {
+            const uint32_t off = rofs + ((g ^ xsw) << 4);
+            float a0, a1, a2, a3;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
+                         : "r"(sX + off)
+                         : "memory");
+            // rank 0 adds (own + peer), rank 1 adds (peer + own): the same two
+            // operands, so both CTAs hold bit-identical scores.
+            si[4 * g] += a0;
+            si[4 * g + 1] += a1;
+            si[4 * g + 2] += a2;
+            si[4 * g + 3] += a3;
+          }
+        }
+        if (alive) {
+          // Our X block may be overwritten once this warp has read it.
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive_remote_cta(ptx::mapa(bar(kBarXFree), peer));
+        }
+      };
+      float s_nx[PAIR ? HB : 1];  // pair: own partial of the next tile, already sent
+      if constexpr (PAIR) {
+        if (count > 0) {
+          load_partial(g0, s_nx);
+          pair_send(g0, s_nx);
+        }
+      }
+
       for (int j = 0; j < count; ++j) {
         const int gt = g0 + j;
         const int tile = w.t_begin + j * w.t_step;
         const int kb = tile * BN + half * HB;  // first key of this thread's columns
-        const int buf = C::QTM ? 0 : (gt & 1);  // S buffer of this tile
+        const int buf = static_cast<int>(static_cast<uint32_t>(gt) % C::NSBUF);  // S buffer
         float s[HB];
 #pragma unroll
         for (int e = 0; e < HB; ++e) s[e] = -INFINITY;
@@ -1214,104 +1335,59 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
             if (kn + HB - 1 < p.Lk) ptx::prefetch_l2(brow + kn + HB - 1);
           }
         }
-        if (alive)
-          alive = __all_sync(0xffffffffu,
-                             wait_bar(bar(kBarSFull + buf), C::QTM ? (gt & 1) : ((gt >> 1) & 1),
-                                      abort_flag, p.status, kDevTimeoutSFull));
-        if (BIAS && !PAIR && alive) {
-          // Scores straight to the log2 domain, c * s + log2(e) * bias, one
-          // 32-column chunk at a time (a masked key becomes -inf below).
-          ptx::tc_fence_after();
-#pragma unroll
-          for (int cch = 0; cch < HB / 32; ++cch) {
-            uint32_t r[32];
-            ptx::tmem_ld32(lane_base + C::S_COL + buf * BN + half * HB + cch * 32, r);
-            ptx::tmem_wait_ld();
-            ptx::reg_fence(r);
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              const float2 bv = unpack2(bw[(cch * 32 + e) / 2], BF16);
-              s[cch * 32 + e] = fmaf(__uint_as_float(r[e]), c, bv.x * kLog2e);
-              s[cch * 32 + e + 1] = fmaf(__uint_as_float(r[e + 1]), c, bv.y * kLog2e);
-            }
-          }
-        } else if (alive) {
-          ptx::tc_fence_after();
-          uint32_t r[HB / 32][32];
-#pragma unroll
-          for (int cch = 0; cch < HB / 32; ++cch)
-            ptx::tmem_ld32(lane_base + C::S_COL + buf * BN + half * HB + cch * 32, r[cch]);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int cch = 0; cch < HB / 32; ++cch) {
-            ptx::reg_fence(r[cch]);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) s[cch * 32 + e] = __uint_as_float(r[cch][e]);
-          }
-        }
-        if constexpr (C::QTM) {
-          // Single S buffer: the next Q.K^T may overwrite it once every softmax
-          // warp has read its lanes (the loads above have completed).
-          if (alive) {
-            ptx::tc_fence_before();
-            warp_arrive(kBarSFree);
-          }
-        }
-
         if constexpr (PAIR) {
-          // Swap partial scores with the peer CTA (same rows and columns) and add
-          // them.  Each warp stages its exchanged rows' HB columns (up to 4 KB) in
-          // XS and one lane bulk-copies the block into the peer's X, completing
-          // the bytes on the peer's XFull barrier; one local arrive per tile posts
-          // the expected byte count for the blocks the peer sends us.
-          const uint32_t wofs = static_cast<uint32_t>(warp) * (32 * HB * 4);
-          const uint32_t rofs = wofs + xidx * (HB * 4);
-          const uint32_t xsw = xidx & (HB / 4 - 1);  // chunk swizzle of this row
-          if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(bar(kBarXFull), xbytes);
-          if (alive)  // our previous block has been received and read by the peer
-            alive = __all_sync(0xffffffffu, wait_bar<true>(bar(kBarXFree), (gt & 1) ^ 1,
-                                                           abort_flag, p.status, kDevTimeoutXFree));
-          if (alive) {
-            if (xrow) {
+          // Own partial of tile j (sent a tile ago) plus the peer's; then send
+          // tile j + 1's partial before this tile's softmax.
 #pragma unroll
-              for (int g = 0; g < HB / 4; ++g) {
-                const uint32_t off = rofs + ((g ^ xsw) << 4);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + C::XS_OFF + off),
-                             "r"(__float_as_uint(s[4 * g])), "r"(__float_as_uint(s[4 * g + 1])),
-                             "r"(__float_as_uint(s[4 * g + 2])), "r"(__float_as_uint(s[4 * g + 3]))
-                             : "memory");
+          for (int e = 0; e < HB; ++e) s[e] = s_nx[e];
+          pair_recv(gt, s);
+          if (j + 1 < count) {
+            load_partial(gt + 1, s_nx);
+            pair_send(gt + 1, s_nx);
+          }
+        } else {
+          if (alive)
+            alive = __all_sync(0xffffffffu,
+                               wait_bar(bar(sfull_bar(buf)), (static_cast<uint32_t>(gt) / C::NSBUF) & 1,
+                                        abort_flag, p.status, kDevTimeoutSFull));
+          if (BIAS && alive) {
+            // Scores straight to the log2 domain, c * s + log2(e) * bias, one
+            // 32-column chunk at a time (a masked key becomes -inf below).
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int cch = 0; cch < HB / 32; ++cch) {
+              uint32_t r[32];
+              ptx::tmem_ld32(lane_base + C::S_COL + buf * BN + half * HB + cch * 32, r);
+              ptx::tmem_wait_ld();
+              ptx::reg_fence(r);
+#pragma unroll
+              for (int e = 0; e < 32; e += 2) {
+                const float2 bv = unpack2(bw[(cch * 32 + e) / 2], BF16);
+                s[cch * 32 + e] = fmaf(__uint_as_float(r[e]), c, bv.x * kLog2e);
+                s[cch * 32 + e + 1] = fmaf(__uint_as_float(r[e + 1]), c, bv.y * kLog2e);
               }
             }
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            const uint32_t nrows = __popc(xmask);
-            if (lane == 0 && nrows > 0)
-              ptx::bulk_copy_to_peer(ptx::mapa(sX + wofs, peer), sbase + C::XS_OFF + wofs,
-                                     nrows * HB * 4, ptx::mapa(bar(kBarXFull), peer));
-            alive = __all_sync(0xffffffffu, wait_bar<true>(bar(kBarXFull), gt & 1, abort_flag,
-                                                           p.status, kDevTimeoutXFull));
-          }
-          if (alive && xrow) {
+          } else if (alive) {
+            ptx::tc_fence_after();
+            uint32_t r[HB / 32][32];
 #pragma unroll
-            for (int g = 0; g < HB / 4; ++g) {
-              const uint32_t off = rofs + ((g ^ xsw) << 4);
-              float a0, a1, a2, a3;
-              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                           : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
-                           : "r"(sX + off)
-                           : "memory");
-              // rank 0 adds (own + peer), rank 1 adds (peer + own): the same two
-              // operands, so both CTAs hold bit-identical scores.
-              s[4 * g] += a0;
-              s[4 * g + 1] += a1;
-              s[4 * g + 2] += a2;
-              s[4 * g + 3] += a3;
+            for (int cch = 0; cch < HB / 32; ++cch)
+              ptx::tmem_ld32(lane_base + C::S_COL + buf * BN + half * HB + cch * 32, r[cch]);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int cch = 0; cch < HB / 32; ++cch) {
+              ptx::reg_fence(r[cch]);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) s[cch * 32 + e] = __uint_as_float(r[cch][e]);
             }
           }
-          if (alive) {
-            // Our X block may be overwritten once this warp has read it.
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive_remote_cta(ptx::mapa(bar(kBarXFree), peer));
+          if constexpr (C::QTM) {
+            // Single S buffer: the next Q.K^T may overwrite it once every softmax
+            // warp has read its lanes (the loads above have completed).
+            if (alive) {
+              ptx::tc_fence_before();
+              warp_arrive(kBarSFree);
+            }
           }
         }
 
