@@ -181,7 +181,7 @@ size_t partial_bytes(long long R, int D, int n_splits) {
 // decode uses one CTA per 16 query heads x 8 position slots and split, the
 // splits of a head group forming a cluster (kDecode) below head_dim 512.
 int choose_mode(bool decode, int D, int window) {
-  if (D == 512) return gbsdpa::kPair;
+  if (D == 512) return gbsdpa::kPairX;
   if (decode) return gbsdpa::kDecode;
   if (D == 192) return gbsdpa::kSingle;
   return (window > 0 && window < 256) ? gbsdpa::kSingle : gbsdpa::kDuo;
@@ -216,7 +216,9 @@ QTiling qtiling(int mode, int G) {
   }
   return t;
 }
-int key_tile(int mode) { return (mode == gbsdpa::kPair || mode == gbsdpa::kDecode) ? 64 : 128; }
+int key_tile(int mode) {
+  return (mode == gbsdpa::kPair || mode == gbsdpa::kPairX || mode == gbsdpa::kDecode) ? 64 : 128;
+}
 
 // Key tiles the longest query tile (of `rows` rows) visits.
 long long max_tiles_per_qtile(int Lq, int Lk, int causal, int window, int bn, int rows) {

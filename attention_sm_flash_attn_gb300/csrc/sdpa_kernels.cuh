@@ -148,11 +148,18 @@ struct AttnParams {
 //            64-key tiles; the splits of a (batch, kv head, head block) form a
 //            thread-block cluster and merge their partials through distributed
 //            shared memory at the end, so one launch writes the output.
-enum Mode : int { kSingle = 0, kPair = 1, kDuo = 2, kDuoQ = 3, kDecode = 4 };
+//   kPairX:  head_dim 512 like kPair, with the work of a tile split between
+//            four exchange warps (they read this CTA's partial scores from
+//            tensor memory and send them to the peer, up to two tiles ahead)
+//            and four softmax warps (one thread per row) that add the two
+//            halves from shared memory; Q in tensor memory, P through shared
+//            memory.
+enum Mode : int { kSingle = 0, kPair = 1, kDuo = 2, kDuoQ = 3, kDecode = 4, kPairX = 5 };
 
 template <bool BF16, int MODE, int HD = 256, int HDV = HD, bool BIAS = false>
 struct Cfg {
-  static constexpr bool PAIR = MODE == kPair;
+  static constexpr bool PX = MODE == kPairX;
+  static constexpr bool PAIR = MODE == kPair || PX;  // head dim split over a CTA pair
   static constexpr bool DUO = MODE == kDuo || MODE == kDuoQ;
   static constexpr bool DEC = MODE == kDecode;
   static constexpr int BM = 128;                   // query rows per CTA
@@ -179,48 +186,63 @@ struct Cfg {
   // Bytes one CTA loads into a ring slot (a V slot is not full below head_dim 256).
   static constexpr int K_SLOT_BYTES = KBOX * KROWS * 128;
   static constexpr int V_SLOT_BYTES = VBOX * V_LBO;
-  static constexpr int Q_OFF = 0;
-  static constexpr int RING_OFF = 65536;
-  // Q in tensor memory (kDuoQ): Q.K^T reads its A operand from TMEM, which
-  // leaves room for one S buffer only, and P goes through shared memory.  The
-  // other variants keep Q in shared memory, two S buffers, and P in TMEM over
-  // the S buffer it came from.
-  static constexpr bool QTM = MODE == kDuoQ;
+  // Q in tensor memory (kDuoQ, kPairX): Q.K^T reads its A operand from TMEM.
+  // P through shared memory (PSM: kDuoQ, kPairX): P.V reads its A operand from
+  // a swizzled shared-memory buffer, and an S buffer is released by its own
+  // barrier (SFREE) once its scores have been read.  The other variants keep Q
+  // in shared memory and P in TMEM over the S buffer it came from.
+  static constexpr bool QTM = MODE == kDuoQ || PX;
+  static constexpr bool PSM = MODE == kDuoQ || PX;
+  static constexpr bool SFREE = PSM;
   // Epilogue through shared memory (STAGE, kDuoQ, in its P buffer): each warp
   // stages 32 rows x 64 columns of the output and writes whole 128-byte lines.
   // (The same staging in the other 2-SM kernel, in a buffer of its own,
   // measured no faster on the sliding-window prefill, so it keeps direct
   // stores and its smaller shared-memory footprint.)
-  static constexpr bool STAGE = QTM;
-  static constexpr int P_OFF = RING_OFF + NSLOT * SLOT;
-  static constexpr int P_BYTES = STAGE ? BM * BN * 2 : 0;
-  static constexpr int X_OFF = P_OFF + P_BYTES;      // peer's partial scores (received)
-  static constexpr int X_BYTES = PAIR ? BM * BN * 4 : 0;
-  static constexpr int XS_OFF = X_OFF + X_BYTES;     // own partial scores (staged to send)
-  static constexpr int BAR_OFF = XS_OFF + X_BYTES;
+  static constexpr bool STAGE = MODE == kDuoQ;
+  // Shared memory.  Most variants: Q tile, ring, [P], [X, XS], barriers, row
+  // swap area, iterators.  kPairX: ring, X (two slots), XS (two slots, which
+  // also stage the query tile before it is copied to TMEM), P, barriers,
+  // iterators.
+  static constexpr int RING_OFF = PX ? 0 : 65536;
+  static constexpr int RING_END = RING_OFF + NSLOT * SLOT;
+  static constexpr int X_SLOTS = PX ? 2 : 1;
+  static constexpr int P_BYTES = PSM ? BM * BN * 2 : 0;
+  static constexpr int X_BYTES = PAIR ? BM * BN * 4 : 0;      // one slot
+  static constexpr int X_OFF = PX ? RING_END : RING_END + P_BYTES;  // peer's partial scores
+  static constexpr int XS_OFF = X_OFF + X_SLOTS * X_BYTES;    // own partial scores to send
+  static constexpr int P_OFF = PX ? XS_OFF + X_SLOTS * X_BYTES : RING_END;
+  static constexpr int Q_OFF = PX ? XS_OFF : 0;
+  static constexpr int BAR_OFF = PX ? P_OFF + P_BYTES : XS_OFF + X_SLOTS * X_BYTES;
   static constexpr int RED_OFF = BAR_OFF + 256;      // [2 parity][2 half][128 rows] floats
+  static constexpr int RED_BYTES = 2048;
   // Piece iterators: softmax warps (state + 2 pieces), producer and MMA issuer
   // (state + 1 piece each), 256 bytes apiece.
-  static constexpr int ITER_OFF = RED_OFF + 2048;
+  static constexpr int ITER_OFF = RED_OFF + RED_BYTES;
   static constexpr int SMEM_BYTES = ITER_OFF + 768;
   static constexpr int S_COL = 256;  // TMEM: O in columns [0,256), S buffers after it
-  // S buffers: kDuoQ has one (released by its own barrier), the head-dim-split
-  // pair three (so the MMA can run two tiles ahead while the softmax swaps
-  // partial scores with the peer), the others two.
-  static constexpr int NSBUF = QTM ? 1 : (PAIR ? 3 : 2);
-  // Q.K^T products the MMA issuer keeps ahead of P.V (every S buffer but the
-  // one P.V reads).
-  static constexpr int S_AHEAD = NSBUF == 3 ? 2 : 1;
+  // S buffers: kDuoQ has one, kPair three (so the MMA can run two tiles ahead
+  // while the softmax swaps partial scores with the peer), the others two.
+  static constexpr int NSBUF = MODE == kDuoQ ? 1 : (MODE == kPair ? 3 : 2);
+  // Q.K^T products the MMA issuer keeps ahead of P.V.
+  static constexpr int S_AHEAD = (MODE == kPair || PX) ? 2 : 1;
   static constexpr int Q_COL = S_COL + NSBUF * BN;   // Q (QTM): DH/2 columns
-  // warps 0-7 softmax (warpgroups 0, 1), 8 producer, 9 MMA, 10-11 idle (warpgroup 2)
-  static constexpr int NTHREADS = 384;
+  // Warps 0-7 softmax (warpgroups 0, 1).  kPairX: 8-11 exchange (warpgroup 2),
+  // 12 producer, 13 MMA, 14-15 idle (warpgroup 3).  Others: 8 producer, 9 MMA,
+  // 10-11 idle (warpgroup 2).
+  static constexpr int NTHREADS = PX ? 512 : 384;
+  static constexpr int kLaunchRegs = PX ? 128 : 168;  // 64K registers / threads, rounded down to 8
   // Registers a thread after the split; the sum stays within the launch
-  // allotment of NTHREADS x 168 (the cap for 12 warps on 4 sub-partitions).
-  static constexpr int kRegsSoftmax = 208;
-  static constexpr int kRegsOther = 88;
-  static_assert(256 * kRegsSoftmax + 128 * kRegsOther <= NTHREADS * 168, "register split");
-  static constexpr int kProducerWarp = 8;
-  static constexpr int kMmaWarp = 9;
+  // allotment of NTHREADS x kLaunchRegs.
+  static constexpr int kRegsSoftmax = PX ? 160 : 208;
+  static constexpr int kRegsExchange = 104;
+  static constexpr int kRegsOther = PX ? 80 : 88;
+  static_assert(256 * kRegsSoftmax + (PX ? 128 * kRegsExchange : 0) + 128 * kRegsOther <=
+                    NTHREADS * kLaunchRegs,
+                "register split");
+  static constexpr int kExchangeWarp = 8;  // kPairX: first exchange warp
+  static constexpr int kProducerWarp = PX ? 12 : 8;
+  static constexpr int kMmaWarp = PX ? 13 : 9;
   static constexpr int MMA_M = DUO ? 256 : 128;
   static constexpr uint32_t IDESC_QK = ptx::idesc_f16(MMA_M, BN, BF16, false, false);
   // P.V: N = DV (the 2-SM variant's B operand is two DV/2-column halves).
@@ -231,13 +253,19 @@ struct Cfg {
   static constexpr int kPFullArrivals = DUO ? 16 : 8;
   static_assert(S_COL + NSBUF * BN + (QTM ? DH / 2 : 0) <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  // Every region the kernel addresses lies inside the window it is launched with.
+  static_assert(RED_OFF + RED_BYTES <= ITER_OFF && ITER_OFF + 768 <= SMEM_BYTES &&
+                    P_OFF + P_BYTES <= (PX ? BAR_OFF : X_OFF) &&
+                    XS_OFF + X_SLOTS * X_BYTES <= (PX ? P_OFF : BAR_OFF),
+                "shared-memory regions overlap");
   static_assert(!STAGE || (P_BYTES >= 8 * 4096 && DV == 256 && !PAIR),
                 "the staged epilogue: 8 warps x 32 rows x 64 columns in the P buffer");
   static_assert(KSUB * KBOX * 64 == DH && VSUB * VROWS == BN, "tile decomposition");
   static_assert(VBOX * 64 == (DUO ? DV / 2 : DV) && V_SLOT_BYTES <= SLOT && K_SLOT_BYTES <= SLOT,
                 "K/V slot layout");
 
-  static_assert(Q_BYTES <= RING_OFF && (!PAIR || (DH == 256 && DV == 256)) && DV <= S_COL,
+  static_assert((PX ? Q_BYTES <= 2 * X_BYTES : Q_BYTES <= RING_OFF) &&
+                    (!PAIR || (DH == 256 && DV == 256)) && DV <= S_COL,
                 "query tile / pair head dim / O columns");
 };
 
@@ -261,6 +289,19 @@ enum {
 static_assert(kNumBars * 8 <= 240, "barriers end below the TMEM slot and abort flag");
 static_assert(sfull_bar(0) == kBarSFull && sfull_bar(1) == kBarSFull + 1 && sfull_bar(2) == kBarSFull2,
               "S-full barriers");
+
+// kPairX's per-slot barriers (its 5-slot ring leaves the ring barriers of slots
+// 5..7 unused, and its two S buffers the third S-full barrier):
+//   xfull   the peer's partial scores landed in our X slot (1 arrival + bytes)
+//   xfree   the peer's softmax warps have read our block from its X slot (8)
+//   sfree   our exchange warps have read S buffer b (4)
+//   xsready our exchange warps have staged our partial scores in XS slot (4)
+//   xsfree  our softmax warps have read XS slot (8)
+__host__ __device__ constexpr int xfull_bar(int x) { return x ? 6 : kBarXFull; }
+__host__ __device__ constexpr int xfree_bar(int x) { return x ? 7 : kBarXFree; }
+__host__ __device__ constexpr int sfree_bar(int b) { return b ? 8 : kBarSFree; }
+__host__ __device__ constexpr int xsready_bar(int x) { return 14 + x; }
+__host__ __device__ constexpr int xsfree_bar(int x) { return x ? kBarSFull2 : 16; }
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 
@@ -620,7 +661,8 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
 // BIAS: add the caller's additive bias (p.bias) to the scores; the kernels
 // without it never read p.bias.
 template <bool BF16, int MODE, int HD, int HDV, bool BIAS = false>
-__global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__((Cfg<BF16, MODE, HD, HDV, BIAS>::NTHREADS), 1)
+    attn_fwd_kernel(const __grid_constant__ AttnParams p) {
   using C = Cfg<BF16, MODE, HD, HDV, BIAS>;
   constexpr bool PAIR = C::PAIR;
   constexpr bool DUO = C::DUO;
@@ -695,15 +737,25 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
       ptx::mbar_init(bar(kBarKvFull + s), 1);
       ptx::mbar_init(bar(kBarKvEmpty + s), 1);
     }
-    for (int b = 0; b < 3; ++b) ptx::mbar_init(bar(sfull_bar(b)), 1);
+    for (int b = 0; b < (C::PX ? 2 : 3); ++b) ptx::mbar_init(bar(sfull_bar(b)), 1);
     ptx::mbar_init(bar(kBarPFull), C::kPFullArrivals);
     ptx::mbar_init(bar(kBarPvDone), 1);
     ptx::mbar_init(bar(kBarQFree), 1);
     ptx::mbar_init(bar(kBarOFree), C::kPFullArrivals);
-    ptx::mbar_init(bar(kBarXFull), 1);  // local expect_tx arrive + the peer's bulk-copy bytes
-    ptx::mbar_init(bar(kBarXFree), 8);  // one arrive per softmax warp of the peer
     ptx::mbar_init(bar(kBarDrain), 1);
-    ptx::mbar_init(bar(kBarSFree), C::kPFullArrivals);
+    if constexpr (C::PX) {
+      for (int x = 0; x < 2; ++x) {
+        ptx::mbar_init(bar(xfull_bar(x)), 1);
+        ptx::mbar_init(bar(xfree_bar(x)), 8);
+        ptx::mbar_init(bar(sfree_bar(x)), 4);
+        ptx::mbar_init(bar(xsready_bar(x)), 4);
+        ptx::mbar_init(bar(xsfree_bar(x)), 8);
+      }
+    } else {
+      ptx::mbar_init(bar(kBarXFull), 1);  // local expect_tx arrive + the peer's bulk-copy bytes
+      ptx::mbar_init(bar(kBarXFree), 8);  // one arrive per softmax warp of the peer
+      ptx::mbar_init(bar(kBarSFree), C::kPFullArrivals);
+    }
     *abort_flag = 0;
     ptx::fence_mbarrier_init();
   }
@@ -810,7 +862,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
   // Warpgroup 2 (producer, MMA issuer, two idle warps) hands its spare
   // registers to the softmax warpgroups; each side changes its budget inside its
   // own branch, so the code after a change is that side's alone.
-  if (warp >= 8) {
+  if (warp >= C::kProducerWarp) {
   ptx::setmaxnreg_dec<C::kRegsOther>();
   if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
@@ -943,10 +995,13 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
         // S_{gt-1}.  Otherwise S buffer gt % 2 last held S_{gt-2} and then
         // P_{gt-2}; the P.V of tile gt - 2 that reads P was issued before this
         // product, and the tensor pipe runs one thread's MMAs in issue order.
-        if constexpr (C::QTM) {
-          if (gt > 0) {
-            if (!wait_bar<DUO>(bar(kBarSFree), (gt - 1) & 1, abort_flag, p.status,
-                               kDevTimeoutSEmpty)) {
+        if constexpr (C::SFREE) {
+          // The S buffer is free once its scores have been read (kDuoQ: by
+          // every softmax warp; kPairX: by the exchange warps).
+          if (gt >= C::NSBUF) {
+            const uint32_t gu = static_cast<uint32_t>(gt);
+            if (!wait_bar<DUO>(bar(sfree_bar(static_cast<int>(gu % C::NSBUF))),
+                               (gu / C::NSBUF - 1) & 1, abort_flag, p.status, kDevTimeoutSEmpty)) {
               ok = false;
               return;
             }
@@ -1011,7 +1066,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
           for (int kk = 0; kk < C::VROWS / 16; ++kk) {
             const int key = vs * C::VROWS + kk * 16;
             const uint64_t b = ptx::sdesc_sw128(sv + kk * 2048, C::V_LBO, 1024);
-            if constexpr (C::QTM) {
+            if constexpr (C::PSM) {
               // A = P_gt in shared memory (K-major, 128B-swizzled, 64 keys a row).
               const uint64_t a =
                   ptx::sdesc_sw128(sP + (key / 64) * 16384 + (key % 64) * 2, 16, 1024);
@@ -1095,6 +1150,94 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
     ptx::cluster_sync();
     ptx::cluster_sync();
   }
+  } else if (C::PX && warp >= C::kExchangeWarp) {
+    ptx::setmaxnreg_dec<C::kRegsExchange>();
+    // ------------------------------------------------------------ exchange (kPairX)
+    // One thread per row (warp 8 + q reads TMEM lanes [32q, 32q + 32)).  Per
+    // key tile j (S buffer and exchange slot j mod 2): read this CTA's partial
+    // scores from TMEM (then the MMA may reuse the buffer), stage them in XS
+    // once our softmax warps and the peer's have read slot j - 2, and
+    // bulk-copy each warp's block into the peer's X slot.  One thread posts the
+    // bytes the peer sends into our X slot.  The softmax warps add the halves.
+    const int q4 = warp & 3;
+    const int t = q4 * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
+    const Work w = make_work<BN, QROWS>(p, item, static_cast<int>(rank));
+    const int count = w.t_count;
+    bool row_valid = true;
+    if (p.decode) {
+      const int hl = t >> 3;
+      const int i = ((((t & 7) - (p.Lk - p.Lq)) % 8) + 8) % 8;
+      row_valid = (i < p.Lq) && (hl < min(p.G, 16)) && (w.h0 + hl < (w.hkv + 1) * p.G);
+    }
+    // Rows whose partial scores go through the exchange: every row in prefill,
+    // the real query rows in decode, packed in row order within each warp.  A
+    // row's BN scores (256 bytes) sit at 16-byte chunk g ^ (position mod 16).
+    const uint32_t xmask = p.decode ? __ballot_sync(0xffffffffu, row_valid) : 0xffffffffu;
+    const uint32_t xidx = __popc(xmask & ((1u << lane) - 1u));
+    const bool xrow = (xmask >> lane) & 1u;
+    const uint32_t nrows = __popc(xmask);
+    constexpr uint32_t RB = BN * 4;
+    const uint32_t wofs = static_cast<uint32_t>(q4) * (32 * RB);
+    const uint32_t rofs = wofs + xidx * RB;
+    const uint32_t xsw = xidx & 15u;
+    uint32_t xbytes = C::X_BYTES;  // bytes the peer sends per tile
+    if (p.decode) {
+      int nv = 0;
+      for (int r = 0; r < 128; ++r) {
+        const int ri = ((((r & 7) - (p.Lk - p.Lq)) % 8) + 8) % 8;
+        nv += (ri < p.Lq) && ((r >> 3) < min(p.G, 16)) && (w.h0 + (r >> 3) < (w.hkv + 1) * p.G);
+      }
+      xbytes = static_cast<uint32_t>(nv) * RB;
+    }
+    auto arrive_local = [&](int barid) {  // one arrival per warp
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(barid));
+    };
+    bool alive = true;
+    for (int j = 0; j < count && alive; ++j) {
+      const int b = j & 1;
+      const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
+      alive = __all_sync(0xffffffffu, wait_bar(bar(sfull_bar(b)), ph, abort_flag, p.status,
+                                               kDevTimeoutSFull));
+      if (!alive) break;
+      ptx::tc_fence_after();
+      uint32_t r0[32], r1[32];
+      ptx::tmem_ld32(lane_base + C::S_COL + b * BN, r0);
+      ptx::tmem_ld32(lane_base + C::S_COL + b * BN + 32, r1);
+      ptx::tmem_wait_ld();
+      ptx::reg_fence(r0);
+      ptx::reg_fence(r1);
+      ptx::tc_fence_before();
+      arrive_local(sfree_bar(b));
+      alive = __all_sync(0xffffffffu, wait_bar(bar(xsfree_bar(b)), ph ^ 1u, abort_flag, p.status,
+                                               kDevTimeoutXFree));
+      if (alive)
+        alive = __all_sync(0xffffffffu, wait_bar<true>(bar(xfree_bar(b)), ph ^ 1u, abort_flag,
+                                                       p.status, kDevTimeoutXFree));
+      if (!alive) break;
+      const uint32_t xs = sbase + C::XS_OFF + static_cast<uint32_t>(b) * C::X_BYTES;
+      if (xrow) {
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           xs + rofs + ((static_cast<uint32_t>(g) ^ xsw) << 4)),
+                       "r"(r0[4 * g]), "r"(r0[4 * g + 1]), "r"(r0[4 * g + 2]), "r"(r0[4 * g + 3])
+                       : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           xs + rofs + ((static_cast<uint32_t>(g + 8) ^ xsw) << 4)),
+                       "r"(r1[4 * g]), "r"(r1[4 * g + 1]), "r"(r1[4 * g + 2]), "r"(r1[4 * g + 3])
+                       : "memory");
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      arrive_local(xsready_bar(b));  // our softmax warps may read the slot
+      if (threadIdx.x == C::kExchangeWarp * 32)
+        ptx::mbar_arrive_expect_tx(bar(xfull_bar(b)), xbytes);
+      if (lane == 0 && nrows > 0)
+        ptx::bulk_copy_to_peer(ptx::mapa(sX + static_cast<uint32_t>(b) * C::X_BYTES + wofs, peer),
+                               xs + wofs, nrows * RB, ptx::mapa(bar(xfull_bar(b)), peer));
+    }
   } else {
     ptx::setmaxnreg_inc<C::kRegsSoftmax>();
     // ------------------------------------------------------------ softmax / epilogue
@@ -1309,7 +1452,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
         }
       };
       float s_nx[PAIR ? HB : 1];  // pair: own partial of the next tile, already sent
-      if constexpr (PAIR) {
+      if constexpr (PAIR && !C::PX) {
         if (count > 0) {
           load_partial(g0, s_nx);
           pair_send(g0, s_nx);
@@ -1335,7 +1478,52 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
             if (kn + HB - 1 < p.Lk) ptx::prefetch_l2(brow + kn + HB - 1);
           }
         }
-        if constexpr (PAIR) {
+        if constexpr (C::PX) {
+          // The exchange warps have staged this CTA's partial scores of tile j
+          // in XS slot j mod 2 and the peer's have landed in X slot j mod 2:
+          // add this thread's half of the row (chunks half * 8 .. of the row's
+          // 16, at chunk g ^ (row position mod 16)), then hand both slots back.
+          const int bx = gt & 1;
+          const uint32_t phx = (static_cast<uint32_t>(gt) >> 1) & 1u;
+          if (alive)
+            alive = __all_sync(0xffffffffu, wait_bar(bar(xsready_bar(bx)), phx, abort_flag,
+                                                     p.status, kDevTimeoutXFull));
+          if (alive)
+            alive = __all_sync(0xffffffffu, wait_bar<true>(bar(xfull_bar(bx)), phx, abort_flag,
+                                                           p.status, kDevTimeoutXFull));
+          if (alive && xrow) {
+            const uint32_t rb = static_cast<uint32_t>(q4) * (32 * BN * 4) + xidx * (BN * 4);
+            const uint32_t xs = sbase + C::XS_OFF + static_cast<uint32_t>(bx) * C::X_BYTES + rb;
+            const uint32_t xr = sX + static_cast<uint32_t>(bx) * C::X_BYTES + rb;
+            const uint32_t sw = xidx & 15u;
+#pragma unroll
+            for (int g = 0; g < HB / 4; ++g) {
+              const uint32_t off = (static_cast<uint32_t>(half * (HB / 4) + g) ^ sw) << 4;
+              float a0, a1, a2, a3, b0, b1, b2, b3;
+              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                           : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
+                           : "r"(xs + off)
+                           : "memory");
+              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                           : "=f"(b0), "=f"(b1), "=f"(b2), "=f"(b3)
+                           : "r"(xr + off)
+                           : "memory");
+              // rank 0 adds (own + peer), rank 1 adds (peer + own): the same
+              // two operands, so both CTAs hold bit-identical scores.
+              s[4 * g] = a0 + b0;
+              s[4 * g + 1] = a1 + b1;
+              s[4 * g + 2] = a2 + b2;
+              s[4 * g + 3] = a3 + b3;
+            }
+          }
+          if (alive) {
+            __syncwarp();
+            if (lane == 0) {
+              ptx::mbar_arrive(bar(xsfree_bar(bx)));
+              ptx::mbar_arrive_remote_cta(ptx::mapa(bar(xfree_bar(bx)), peer));
+            }
+          }
+        } else if constexpr (PAIR) {
           // Own partial of tile j (sent a tile ago) plus the peer's; then send
           // tile j + 1's partial before this tile's softmax.
 #pragma unroll
@@ -1480,7 +1668,7 @@ __global__ void __launch_bounds__(384, 1) attn_fwd_kernel(const __grid_constant_
           }
           ptx::tmem_wait_st();
         }
-        if constexpr (C::QTM) {
+        if constexpr (C::PSM) {
           // P row -> shared memory, K-major 128B-swizzled (64 keys per 128-byte row).
 #pragma unroll
           for (int ch = 0; ch < HB / 8; ++ch) {

@@ -18,14 +18,14 @@ using gbsdpa::AttnParams;
 using gbsdpa::Cfg;
 
 // Slot of a kernel instantiation in the per-device tables: bias x dtype x
-// variant (5) x per-CTA head dims (Q/K, V): (256, 256), (128, 128), (192, 192),
+// variant (6) x per-CTA head dims (Q/K, V): (256, 256), (128, 128), (192, 192),
 // (192, 256).
 template <bool BF16, int MODE, int HD, int HDV, bool BIAS>
 constexpr int variant_index() {
-  return (BIAS ? 40 : 0) + (BF16 ? 1 : 0) +
+  return (BIAS ? 48 : 0) + (BF16 ? 1 : 0) +
          2 * (MODE * 4 + (HD != HDV ? 3 : HD == 256 ? 0 : HD == 128 ? 1 : 2));
 }
-constexpr int kNumVariants = 2 * 2 * 5 * 4;
+constexpr int kNumVariants = 2 * 2 * 6 * 4;
 
 struct DeviceState {
   bool ready = false;
@@ -190,6 +190,7 @@ int launch_variant(int mode, int D, int Dv, const AttnParams& p, long long items
   using gbsdpa::kSingle;
   switch (mode) {
     case kPair: return launch_attn<BF16, kPair, 256, 256, BIAS>(p, items, stream, st);
+    case gbsdpa::kPairX: return launch_attn<BF16, gbsdpa::kPairX, 256, 256, BIAS>(p, items, stream, st);
     case kDuoQ:
       if constexpr (!BIAS)
         return launch_attn<BF16, kDuoQ, 256, 256, false>(p, items, stream, st);
