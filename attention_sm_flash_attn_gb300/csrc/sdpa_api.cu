@@ -143,15 +143,13 @@ int validate_kv_layout(int Lq, int Lk, int causal, int window, int kv_cap, int k
 
 int launch_combine(const float* part_o, const float* part_ml, void* out, long long R, int D,
                    int n_splits, bool bf16, cudaStream_t stream) {
-  // weights (n_splits + 1, padded to 4 floats) then 8 x 32 float4 warp sums
-  const size_t sh = static_cast<size_t>((n_splits + 4) & ~3) * sizeof(float) + 8 * 32 * 16;
   if (R <= 0 || R > 0x7fffffffll || D % 64 != 0) return SDPA_ERR_INVALID_ARG;
   // Programmatic dependent launch: the merge grid's CTAs may be placed while the
   // attention grid drains; the kernel waits for that grid before reading.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(R), static_cast<unsigned>((D + 127) / 128));
   cfg.blockDim = dim3(gbsdpa::kCombineThreads, 1, 1);
-  cfg.dynamicSmemBytes = sh;
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -181,7 +179,7 @@ size_t partial_bytes(long long R, int D, int n_splits) {
 // decode uses one CTA per 16 query heads x 8 position slots and split, the
 // splits of a head group forming a cluster (kDecode) below head_dim 512.
 int choose_mode(bool decode, int D, int window) {
-  if (D == 512) return gbsdpa::kPairX;
+  if (D == 512) return decode ? gbsdpa::kPairXD : gbsdpa::kPairX;
   if (decode) return gbsdpa::kDecode;
   if (D == 192) return gbsdpa::kSingle;
   return (window > 0 && window < 256) ? gbsdpa::kSingle : gbsdpa::kDuo;
@@ -217,7 +215,8 @@ QTiling qtiling(int mode, int G) {
   return t;
 }
 int key_tile(int mode) {
-  return (mode == gbsdpa::kPair || mode == gbsdpa::kPairX || mode == gbsdpa::kDecode) ? 64 : 128;
+  return (mode == gbsdpa::kPairX || mode == gbsdpa::kPairXD || mode == gbsdpa::kDecode) ? 64
+                                                                                       : 128;
 }
 
 // Key tiles the longest query tile (of `rows` rows) visits.

@@ -51,8 +51,8 @@
 
 namespace gbsdpa {
 
-// Barrier that signals "S buffer `buf` holds a finished Q.K^T product".
-__host__ __device__ constexpr int sfull_bar(int buf) { return buf < 2 ? 17 + buf : 27; }
+// Barrier that signals "S buffer `buf` (0 or 1) holds a finished Q.K^T product".
+__host__ __device__ constexpr int sfull_bar(int buf) { return 17 + buf; }
 
 // Device status codes (bit pattern identifies the wait that gave up).
 enum : int {
@@ -137,8 +137,6 @@ struct AttnParams {
 
 // Kernel variants.
 //   kSingle: one CTA per 128 query rows, head_dim 256 (decode, and prefill fallback).
-//   kPair:   head_dim 512; a 2-CTA cluster splits the head dimension and swaps
-//            partial scores through distributed shared memory.
 //   kDuo:    head_dim 256 prefill with 2-SM MMAs (cta_group::2): a 2-CTA
 //            cluster owns 256 query rows; each CTA loads half of every K and V
 //            tile, which halves the bytes each SM stages per FLOP.
@@ -148,18 +146,25 @@ struct AttnParams {
 //            64-key tiles; the splits of a (batch, kv head, head block) form a
 //            thread-block cluster and merge their partials through distributed
 //            shared memory at the end, so one launch writes the output.
-//   kPairX:  head_dim 512 like kPair, with the work of a tile split between
-//            four exchange warps (they read this CTA's partial scores from
-//            tensor memory and send them to the peer, up to two tiles ahead)
-//            and four softmax warps (one thread per row) that add the two
-//            halves from shared memory; Q in tensor memory, P through shared
-//            memory.
-enum Mode : int { kSingle = 0, kPair = 1, kDuo = 2, kDuoQ = 3, kDecode = 4, kPairX = 5 };
+//   kPairX:  head_dim 512: a 2-CTA cluster splits the head dimension and swaps
+//            partial scores through distributed shared memory.  Four exchange
+//            warps read this CTA's partial scores from tensor memory and send
+//            them to the peer (up to two tiles ahead); eight softmax warps add
+//            the two halves from shared memory.  Q in tensor memory, P through
+//            shared memory.
+//   kPairXD: kPairX for decode (Lq <= 8): an 8-slot K/V ring and one exchange
+//            slot instead of a 5-slot ring and two, which keeps more of the
+//            K/V stream in flight (the prefill kernel measured slower with it).
+// (Value 1 belonged to an earlier head_dim-512 pair that the exchange warps
+// replaced; the numbers of the others are kept.)
+enum Mode : int { kSingle = 0, kDuo = 2, kDuoQ = 3, kDecode = 4, kPairX = 5, kPairXD = 6 };
+constexpr int kNumModes = 7;
 
 template <bool BF16, int MODE, int HD = 256, int HDV = HD, bool BIAS = false>
 struct Cfg {
-  static constexpr bool PX = MODE == kPairX;
-  static constexpr bool PAIR = MODE == kPair || PX;  // head dim split over a CTA pair
+  static constexpr bool PX = MODE == kPairX || MODE == kPairXD;
+  static constexpr bool PXD = MODE == kPairXD;
+  static constexpr bool PAIR = PX;  // head dim split over a CTA pair
   static constexpr bool DUO = MODE == kDuo || MODE == kDuoQ;
   static constexpr bool DEC = MODE == kDecode;
   static constexpr int BM = 128;                   // query rows per CTA
@@ -167,7 +172,7 @@ struct Cfg {
   static constexpr int DV = HDV;                   // V (and output) head-dim columns
   static constexpr int BN = (PAIR || DEC) ? 64 : 128;  // keys per tile
   static constexpr int HB = BN / 2;                // key columns per softmax thread
-  static constexpr int NSLOT = PAIR ? 5 : 8;
+  static constexpr int NSLOT = (PX && !PXD) ? 5 : 8;
   static constexpr int SLOT = 16384;
   // K per CTA and tile: DUO holds 64 of the 128 keys, the others all BN keys.
   static constexpr int KROWS = DUO ? 64 : BN;      // rows of a K box
@@ -200,20 +205,23 @@ struct Cfg {
   // measured no faster on the sliding-window prefill, so it keeps direct
   // stores and its smaller shared-memory footprint.)
   static constexpr bool STAGE = MODE == kDuoQ;
-  // Shared memory.  Most variants: Q tile, ring, [P], [X, XS], barriers, row
-  // swap area, iterators.  kPairX: ring, X (two slots), XS (two slots, which
-  // also stage the query tile before it is copied to TMEM), P, barriers,
-  // iterators.
+  // Shared memory.  Most variants: Q tile, ring, [P], barriers, row swap
+  // area, iterators.  kPairX: ring (5 slots), X and XS (two slots each), P,
+  // barriers, row swap area, iterators.  kPairXD: ring (8 slots), X, XS, P,
+  // 16 KB spare, barriers, ...  The pairs stage the query tile over XS (and
+  // P and the spare) before it is copied to TMEM: those are first written
+  // after the first Q.K^T, which follows that copy.
   static constexpr int RING_OFF = PX ? 0 : 65536;
   static constexpr int RING_END = RING_OFF + NSLOT * SLOT;
-  static constexpr int X_SLOTS = PX ? 2 : 1;
+  static constexpr int X_SLOTS = (PX && !PXD) ? 2 : 1;  // exchange slots (X and XS)
   static constexpr int P_BYTES = PSM ? BM * BN * 2 : 0;
   static constexpr int X_BYTES = PAIR ? BM * BN * 4 : 0;      // one slot
   static constexpr int X_OFF = PX ? RING_END : RING_END + P_BYTES;  // peer's partial scores
   static constexpr int XS_OFF = X_OFF + X_SLOTS * X_BYTES;    // own partial scores to send
   static constexpr int P_OFF = PX ? XS_OFF + X_SLOTS * X_BYTES : RING_END;
   static constexpr int Q_OFF = PX ? XS_OFF : 0;
-  static constexpr int BAR_OFF = PX ? P_OFF + P_BYTES : XS_OFF + X_SLOTS * X_BYTES;
+  static constexpr int BAR_OFF =
+      PX ? P_OFF + P_BYTES + (PXD ? 16384 : 0) : XS_OFF + X_SLOTS * X_BYTES;
   static constexpr int RED_OFF = BAR_OFF + 256;      // [2 parity][2 half][128 rows] floats
   static constexpr int RED_BYTES = 2048;
   // Piece iterators: softmax warps (state + 2 pieces), producer and MMA issuer
@@ -221,11 +229,11 @@ struct Cfg {
   static constexpr int ITER_OFF = RED_OFF + RED_BYTES;
   static constexpr int SMEM_BYTES = ITER_OFF + 768;
   static constexpr int S_COL = 256;  // TMEM: O in columns [0,256), S buffers after it
-  // S buffers: kDuoQ has one, kPair three (so the MMA can run two tiles ahead
-  // while the softmax swaps partial scores with the peer), the others two.
-  static constexpr int NSBUF = MODE == kDuoQ ? 1 : (MODE == kPair ? 3 : 2);
-  // Q.K^T products the MMA issuer keeps ahead of P.V.
-  static constexpr int S_AHEAD = (MODE == kPair || PX) ? 2 : 1;
+  // S buffers: kDuoQ has one, the others two.
+  static constexpr int NSBUF = MODE == kDuoQ ? 1 : 2;
+  // Q.K^T products the MMA issuer keeps ahead of P.V (the pair runs two tiles
+  // ahead while the exchange warps swap partial scores with the peer).
+  static constexpr int S_AHEAD = PX ? 2 : 1;
   static constexpr int Q_COL = S_COL + NSBUF * BN;   // Q (QTM): DH/2 columns
   // Warps 0-7 softmax (warpgroups 0, 1).  kPairX: 8-11 exchange (warpgroup 2),
   // 12 producer, 13 MMA, 14-15 idle (warpgroup 3).  Others: 8 producer, 9 MMA,
@@ -258,6 +266,7 @@ struct Cfg {
                     P_OFF + P_BYTES <= (PX ? BAR_OFF : X_OFF) &&
                     XS_OFF + X_SLOTS * X_BYTES <= (PX ? P_OFF : BAR_OFF),
                 "shared-memory regions overlap");
+  static_assert(!PX || Q_OFF + Q_BYTES <= BAR_OFF, "query staging over XS, P and the spare");
   static_assert(!STAGE || (P_BYTES >= 8 * 4096 && DV == 256 && !PAIR),
                 "the staged epilogue: 8 warps x 32 rows x 64 columns in the P buffer");
   static_assert(KSUB * KBOX * 64 == DH && VSUB * VROWS == BN, "tile decomposition");
@@ -283,15 +292,14 @@ enum {
   kBarXFree = 24,
   kBarDrain = 25,
   kBarSFree = 26,    // Q in TMEM: the softmax has read the (single) S buffer
-  kBarSFull2 = 27,   // third S buffer (head-dim-split pair)
-  kNumBars = 28,
+  kNumBars = 30,     // 27..29: kPairX exchange barriers (below)
 };
 static_assert(kNumBars * 8 <= 240, "barriers end below the TMEM slot and abort flag");
-static_assert(sfull_bar(0) == kBarSFull && sfull_bar(1) == kBarSFull + 1 && sfull_bar(2) == kBarSFull2,
-              "S-full barriers");
+static_assert(sfull_bar(0) == kBarSFull && sfull_bar(1) == kBarSFull + 1, "S-full barriers");
 
-// kPairX's per-slot barriers (its 5-slot ring leaves the ring barriers of slots
-// 5..7 unused, and its two S buffers the third S-full barrier):
+// The pairs' exchange barriers, per exchange slot x (NX = 2 slots: kPairX,
+// whose 5-slot ring leaves the ring barriers of slots 5..7 free; NX = 1:
+// kPairXD, 8 ring slots) and S buffer b:
 //   xfull   the peer's partial scores landed in our X slot (1 arrival + bytes)
 //   xfree   the peer's softmax warps have read our block from its X slot (8)
 //   sfree   our exchange warps have read S buffer b (4)
@@ -299,9 +307,12 @@ static_assert(sfull_bar(0) == kBarSFull && sfull_bar(1) == kBarSFull + 1 && sful
 //   xsfree  our softmax warps have read XS slot (8)
 __host__ __device__ constexpr int xfull_bar(int x) { return x ? 6 : kBarXFull; }
 __host__ __device__ constexpr int xfree_bar(int x) { return x ? 7 : kBarXFree; }
-__host__ __device__ constexpr int sfree_bar(int b) { return b ? 8 : kBarSFree; }
-__host__ __device__ constexpr int xsready_bar(int x) { return 14 + x; }
-__host__ __device__ constexpr int xsfree_bar(int x) { return x ? kBarSFull2 : 16; }
+template <int NX>
+__host__ __device__ constexpr int sfree_bar(int b) { return b ? (NX == 2 ? 8 : 27) : kBarSFree; }
+template <int NX>
+__host__ __device__ constexpr int xsready_bar(int x) { return NX == 2 ? 14 + x : 28; }
+template <int NX>
+__host__ __device__ constexpr int xsfree_bar(int x) { return NX == 2 ? (x ? 27 : 16) : 29; }
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 
@@ -737,20 +748,20 @@ __global__ void __launch_bounds__((Cfg<BF16, MODE, HD, HDV, BIAS>::NTHREADS), 1)
       ptx::mbar_init(bar(kBarKvFull + s), 1);
       ptx::mbar_init(bar(kBarKvEmpty + s), 1);
     }
-    for (int b = 0; b < (C::PX ? 2 : 3); ++b) ptx::mbar_init(bar(sfull_bar(b)), 1);
+    for (int b = 0; b < 2; ++b) ptx::mbar_init(bar(sfull_bar(b)), 1);
     ptx::mbar_init(bar(kBarPFull), C::kPFullArrivals);
     ptx::mbar_init(bar(kBarPvDone), 1);
     ptx::mbar_init(bar(kBarQFree), 1);
     ptx::mbar_init(bar(kBarOFree), C::kPFullArrivals);
     ptx::mbar_init(bar(kBarDrain), 1);
     if constexpr (C::PX) {
-      for (int x = 0; x < 2; ++x) {
+      for (int x = 0; x < C::X_SLOTS; ++x) {
         ptx::mbar_init(bar(xfull_bar(x)), 1);
         ptx::mbar_init(bar(xfree_bar(x)), 8);
-        ptx::mbar_init(bar(sfree_bar(x)), 4);
-        ptx::mbar_init(bar(xsready_bar(x)), 4);
-        ptx::mbar_init(bar(xsfree_bar(x)), 8);
+        ptx::mbar_init(bar(xsready_bar<C::X_SLOTS>(x)), 4);
+        ptx::mbar_init(bar(xsfree_bar<C::X_SLOTS>(x)), 8);
       }
+      for (int b = 0; b < 2; ++b) ptx::mbar_init(bar(sfree_bar<C::X_SLOTS>(b)), 4);
     } else {
       ptx::mbar_init(bar(kBarXFull), 1);  // local expect_tx arrive + the peer's bulk-copy bytes
       ptx::mbar_init(bar(kBarXFree), 8);  // one arrive per softmax warp of the peer
@@ -1000,7 +1011,7 @@ __global__ void __launch_bounds__((Cfg<BF16, MODE, HD, HDV, BIAS>::NTHREADS), 1)
           // every softmax warp; kPairX: by the exchange warps).
           if (gt >= C::NSBUF) {
             const uint32_t gu = static_cast<uint32_t>(gt);
-            if (!wait_bar<DUO>(bar(sfree_bar(static_cast<int>(gu % C::NSBUF))),
+            if (!wait_bar<DUO>(bar(sfree_bar<C::X_SLOTS>(static_cast<int>(gu % C::NSBUF))),
                                (gu / C::NSBUF - 1) & 1, abort_flag, p.status, kDevTimeoutSEmpty)) {
               ok = false;
               return;
@@ -1129,11 +1140,11 @@ __global__ void __launch_bounds__((Cfg<BF16, MODE, HD, HDV, BIAS>::NTHREADS), 1)
           const int pro = min(count, C::S_AHEAD);
           for (int j = 0; j < pro && ok; ++j) {
             do_s(g0 + j);
-            if (ok && j == count - 1) commit(kBarQFree);
+            if (!C::QTM && ok && j == count - 1) commit(kBarQFree);
           }
           for (int j = C::S_AHEAD; j < count && ok; ++j) {
             do_s(g0 + j);
-            if (ok && j == count - 1) commit(kBarQFree);
+            if (!C::QTM && ok && j == count - 1) commit(kBarQFree);
             if (ok) do_pv(g0 + j - C::S_AHEAD, j - C::S_AHEAD);
           }
           for (int j = count - pro; j < count && ok; ++j) do_pv(g0 + j, j);
@@ -1154,11 +1165,14 @@ __global__ void __launch_bounds__((Cfg<BF16, MODE, HD, HDV, BIAS>::NTHREADS), 1)
     ptx::setmaxnreg_dec<C::kRegsExchange>();
     // ------------------------------------------------------------ exchange (kPairX)
     // One thread per row (warp 8 + q reads TMEM lanes [32q, 32q + 32)).  Per
-    // key tile j (S buffer and exchange slot j mod 2): read this CTA's partial
-    // scores from TMEM (then the MMA may reuse the buffer), stage them in XS
-    // once our softmax warps and the peer's have read slot j - 2, and
-    // bulk-copy each warp's block into the peer's X slot.  One thread posts the
-    // bytes the peer sends into our X slot.  The softmax warps add the halves.
+    // key tile j (S buffer j mod 2, exchange slot j mod X_SLOTS): read this
+    // CTA's partial scores from TMEM (then the MMA may reuse the buffer), stage
+    // them in XS once our softmax warps and the peer's have read the slot's
+    // previous tile, and bulk-copy each warp's block into the peer's X slot.
+    // One thread posts the bytes the peer sends into our X slot.  The softmax
+    // warps add the halves.  (One slot: shared memory goes to an 8-slot ring,
+    // which keeps more of a decode's K/V loads in flight; two slots measured
+    // no faster in prefill.)
     const int q4 = warp & 3;
     const int t = q4 * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
@@ -1196,8 +1210,10 @@ __global__ void __launch_bounds__((Cfg<BF16, MODE, HD, HDV, BIAS>::NTHREADS), 1)
     };
     bool alive = true;
     for (int j = 0; j < count && alive; ++j) {
-      const int b = j & 1;
+      const int b = j & 1;  // S buffer
       const uint32_t ph = static_cast<uint32_t>(j >> 1) & 1u;
+      const int xb = j % C::X_SLOTS;  // X / XS slot
+      const uint32_t xph = static_cast<uint32_t>(j / C::X_SLOTS) & 1u;
       alive = __all_sync(0xffffffffu, wait_bar(bar(sfull_bar(b)), ph, abort_flag, p.status,
                                                kDevTimeoutSFull));
       if (!alive) break;
@@ -1209,14 +1225,14 @@ __global__ void __launch_bounds__((Cfg<BF16, MODE, HD, HDV, BIAS>::NTHREADS), 1)
       ptx::reg_fence(r0);
       ptx::reg_fence(r1);
       ptx::tc_fence_before();
-      arrive_local(sfree_bar(b));
-      alive = __all_sync(0xffffffffu, wait_bar(bar(xsfree_bar(b)), ph ^ 1u, abort_flag, p.status,
-                                               kDevTimeoutXFree));
+      arrive_local(sfree_bar<C::X_SLOTS>(b));
+      alive = __all_sync(0xffffffffu, wait_bar(bar(xsfree_bar<C::X_SLOTS>(xb)), xph ^ 1u,
+                                               abort_flag, p.status, kDevTimeoutXFree));
       if (alive)
-        alive = __all_sync(0xffffffffu, wait_bar<true>(bar(xfree_bar(b)), ph ^ 1u, abort_flag,
+        alive = __all_sync(0xffffffffu, wait_bar<true>(bar(xfree_bar(xb)), xph ^ 1u, abort_flag,
                                                        p.status, kDevTimeoutXFree));
       if (!alive) break;
-      const uint32_t xs = sbase + C::XS_OFF + static_cast<uint32_t>(b) * C::X_BYTES;
+      const uint32_t xs = sbase + C::XS_OFF + static_cast<uint32_t>(xb) * C::X_BYTES;
       if (xrow) {
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
@@ -1231,12 +1247,12 @@ __global__ void __launch_bounds__((Cfg<BF16, MODE, HD, HDV, BIAS>::NTHREADS), 1)
         }
       }
       ptx::fence_proxy_async_smem();
-      arrive_local(xsready_bar(b));  // our softmax warps may read the slot
+      arrive_local(xsready_bar<C::X_SLOTS>(xb));  // our softmax warps may read the slot
       if (threadIdx.x == C::kExchangeWarp * 32)
-        ptx::mbar_arrive_expect_tx(bar(xfull_bar(b)), xbytes);
+        ptx::mbar_arrive_expect_tx(bar(xfull_bar(xb)), xbytes);
       if (lane == 0 && nrows > 0)
-        ptx::bulk_copy_to_peer(ptx::mapa(sX + static_cast<uint32_t>(b) * C::X_BYTES + wofs, peer),
-                               xs + wofs, nrows * RB, ptx::mapa(bar(xfull_bar(b)), peer));
+        ptx::bulk_copy_to_peer(ptx::mapa(sX + static_cast<uint32_t>(xb) * C::X_BYTES + wofs, peer),
+                               xs + wofs, nrows * RB, ptx::mapa(bar(xfull_bar(xb)), peer));
     }
   } else {
     ptx::setmaxnreg_inc<C::kRegsSoftmax>();
@@ -1324,9 +1340,26 @@ __global__ void __launch_bounds__((Cfg<BF16, MODE, HD, HDV, BIAS>::NTHREADS), 1)
         if (count > 0) {
           // Decode: stage this thread's half of the row's query slice into the
           // swizzled Q tile (16-byte chunks of 8 elements); kDecode issued
-          // these copies at entry and only waits for them here.
+          // these copies at entry and only waits for them here, kPairXD
+          // issues all of a thread's loads before its first store.
           if constexpr (C::DEC) {
             ptx::cp_async_wait_all();
+          } else if constexpr (C::PXD) {
+            const uint4* src =
+                reinterpret_cast<const uint4*>(p.q + row_id * p.Dqk + d0) + half * (C::DH / 16);
+            uint4 v[C::DH / 16];
+#pragma unroll
+            for (int c = 0; c < C::DH / 16; ++c)
+              v[c] = row_valid ? src[c] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int c = 0; c < C::DH / 16; ++c) {
+              const int cq = half * (C::DH / 16) + c;
+              const int dc = cq >> 3, cc = cq & 7;
+              const uint32_t addr = sQ + dc * 16384 + t * 128 + ((cc ^ (t & 7)) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[c].x),
+                           "r"(v[c].y), "r"(v[c].z), "r"(v[c].w)
+                           : "memory");
+            }
           } else {
             const uint4* src = reinterpret_cast<const uint4*>(p.q + row_id * p.Dqk + d0);
             for (int cq = half * (C::DH / 16); cq < (half + 1) * (C::DH / 16); ++cq) {
@@ -1345,119 +1378,16 @@ __global__ void __launch_bounds__((Cfg<BF16, MODE, HD, HDV, BIAS>::NTHREADS), 1)
         }
       }
 
-      // Pair: rows of this warp whose partial scores go through the exchange.  In
-      // decode only the real query rows do (16 x Lq of the 128), packed in row
-      // order; both CTAs of the pair hold the same rows, so they agree on the
-      // packing.  `xbytes` (thread 0) is what the peer sends per tile.
-      uint32_t xmask = 0xffffffffu;
-      uint32_t xbytes = C::X_BYTES;
-      if (PAIR && p.decode) {
-        xmask = __ballot_sync(0xffffffffu, row_valid);
-        if (threadIdx.x == 0) {
-          int nv = 0;
-          for (int r = 0; r < 128; ++r) {
-            const int ri = ((((r & 7) - (p.Lk - p.Lq)) % 8) + 8) % 8;
-            nv += (ri < p.Lq) && ((r >> 3) < min(p.G, 16)) &&
-                  (w.h0 + (r >> 3) < (w.hkv + 1) * p.G);
-          }
-          xbytes = static_cast<uint32_t>(nv) * BN * 4;  // both column halves of each row
-        }
-      }
+      // Pair: rows of this warp whose partial scores go through the exchange
+      // (the exchange warps pack them the same way): every row in prefill, the
+      // real query rows in decode (16 x Lq of the 128), in row order.
+      const uint32_t xmask =
+          (PAIR && p.decode) ? __ballot_sync(0xffffffffu, row_valid) : 0xffffffffu;
       const uint32_t xidx = __popc(xmask & ((1u << lane) - 1u));  // packed position
       const bool xrow = (xmask >> lane) & 1u;
 
       float m_run = -INFINITY;  // running max of c * s (lazy: the true max may exceed it by < 8)
       float l = 0.f;            // this half's share of the row sum
-
-      // Pair: this CTA's partial scores of a tile go to the peer one tile ahead
-      // of the softmax that needs them.  send(gx) waits for S_gx, loads this
-      // CTA's partial (kept in registers for the add), stages the exchanged
-      // rows' HB columns (up to 4 KB a warp) in XS and one lane bulk-copies the
-      // block into the peer's X, completing the bytes on the peer's XFull
-      // barrier (thread 0 posts the expected byte count of the peer's block on
-      // ours).  recv(gx) waits for the peer's block, adds it and hands X back.
-      // Tile j's softmax runs while tile j + 1's blocks are in flight.
-      const uint32_t wofs = static_cast<uint32_t>(warp) * (32 * HB * 4);
-      const uint32_t rofs = wofs + xidx * (HB * 4);
-      const uint32_t xsw = xidx & (HB / 4 - 1);  // chunk swizzle of this row
-      auto load_partial = [&](int gx, float (&so)[HB]) {
-        const int bx = static_cast<int>(static_cast<uint32_t>(gx) % C::NSBUF);
-        if (alive)
-          alive = __all_sync(0xffffffffu,
-                             wait_bar(bar(sfull_bar(bx)), (static_cast<uint32_t>(gx) / C::NSBUF) & 1,
-                                      abort_flag, p.status, kDevTimeoutSFull));
-        if (alive) {
-          ptx::tc_fence_after();
-          uint32_t r[32];
-          ptx::tmem_ld32(lane_base + C::S_COL + bx * BN + half * HB, r);
-          ptx::tmem_wait_ld();
-          ptx::reg_fence(r);
-#pragma unroll
-          for (int e = 0; e < HB; ++e) so[e] = __uint_as_float(r[e]);
-        }
-      };
-      auto pair_send = [&](int gx, const float (&so)[HB]) {
-        // Exactly one arrival per phase of XFull: once a wait of this warp has
-        // given up, no further phase is waited for, and none is posted (a
-        // second arrival on a phase whose arrival is in would drive its
-        // pending count below zero).
-        if (threadIdx.x == 0 && alive) ptx::mbar_arrive_expect_tx(bar(kBarXFull), xbytes);
-        if (alive)  // the peer has read our previous block (and so it has landed)
-          alive = __all_sync(0xffffffffu, wait_bar<true>(bar(kBarXFree), (gx & 1) ^ 1, abort_flag,
-                                                         p.status, kDevTimeoutXFree));
-        if (alive) {
-          if (xrow) {
-#pragma unroll
-            for (int g = 0; g < HB / 4; ++g) {
-              const uint32_t off = rofs + ((g ^ xsw) << 4);
-              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + C::XS_OFF + off),
-                           "r"(__float_as_uint(so[4 * g])), "r"(__float_as_uint(so[4 * g + 1])),
-                           "r"(__float_as_uint(so[4 * g + 2])), "r"(__float_as_uint(so[4 * g + 3]))
-                           : "memory");
-            }
-          }
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          const uint32_t nrows = __popc(xmask);
-          if (lane == 0 && nrows > 0)
-            ptx::bulk_copy_to_peer(ptx::mapa(sX + wofs, peer), sbase + C::XS_OFF + wofs,
-                                   nrows * HB * 4, ptx::mapa(bar(kBarXFull), peer));
-        }
-      };
-      auto pair_recv = [&](int gx, float (&si)[HB]) {
-        if (alive)
-          alive = __all_sync(0xffffffffu, wait_bar<true>(bar(kBarXFull), gx & 1, abort_flag,
-                                                         p.status, kDevTimeoutXFull));
-        if (alive && xrow) {
-#pragma unroll
-          for (int g = 0; g < HB / 4; ++g) {
-            const uint32_t off = rofs + ((g ^ xsw) << 4);
-            float a0, a1, a2, a3;
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
-                         : "r"(sX + off)
-                         : "memory");
-            // rank 0 adds (own + peer), rank 1 adds (peer + own): the same two
-            // operands, so both CTAs hold bit-identical scores.
-            si[4 * g] += a0;
-            si[4 * g + 1] += a1;
-            si[4 * g + 2] += a2;
-            si[4 * g + 3] += a3;
-          }
-        }
-        if (alive) {
-          // Our X block may be overwritten once this warp has read it.
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive_remote_cta(ptx::mapa(bar(kBarXFree), peer));
-        }
-      };
-      float s_nx[PAIR ? HB : 1];  // pair: own partial of the next tile, already sent
-      if constexpr (PAIR && !C::PX) {
-        if (count > 0) {
-          load_partial(g0, s_nx);
-          pair_send(g0, s_nx);
-        }
-      }
 
       for (int j = 0; j < count; ++j) {
         const int gt = g0 + j;
@@ -1480,13 +1410,13 @@ __global__ void __launch_bounds__((Cfg<BF16, MODE, HD, HDV, BIAS>::NTHREADS), 1)
         }
         if constexpr (C::PX) {
           // The exchange warps have staged this CTA's partial scores of tile j
-          // in XS slot j mod 2 and the peer's have landed in X slot j mod 2:
+          // in XS slot j mod X_SLOTS and the peer's have landed in that X slot:
           // add this thread's half of the row (chunks half * 8 .. of the row's
           // 16, at chunk g ^ (row position mod 16)), then hand both slots back.
-          const int bx = gt & 1;
-          const uint32_t phx = (static_cast<uint32_t>(gt) >> 1) & 1u;
+          const int bx = gt % C::X_SLOTS;
+          const uint32_t phx = static_cast<uint32_t>(gt / C::X_SLOTS) & 1u;
           if (alive)
-            alive = __all_sync(0xffffffffu, wait_bar(bar(xsready_bar(bx)), phx, abort_flag,
+            alive = __all_sync(0xffffffffu, wait_bar(bar(xsready_bar<C::X_SLOTS>(bx)), phx, abort_flag,
                                                      p.status, kDevTimeoutXFull));
           if (alive)
             alive = __all_sync(0xffffffffu, wait_bar<true>(bar(xfull_bar(bx)), phx, abort_flag,
@@ -1519,19 +1449,9 @@ __global__ void __launch_bounds__((Cfg<BF16, MODE, HD, HDV, BIAS>::NTHREADS), 1)
           if (alive) {
             __syncwarp();
             if (lane == 0) {
-              ptx::mbar_arrive(bar(xsfree_bar(bx)));
+              ptx::mbar_arrive(bar(xsfree_bar<C::X_SLOTS>(bx)));
               ptx::mbar_arrive_remote_cta(ptx::mapa(bar(xfree_bar(bx)), peer));
             }
-          }
-        } else if constexpr (PAIR) {
-          // Own partial of tile j (sent a tile ago) plus the peer's; then send
-          // tile j + 1's partial before this tile's softmax.
-#pragma unroll
-          for (int e = 0; e < HB; ++e) s[e] = s_nx[e];
-          pair_recv(gt, s);
-          if (j + 1 < count) {
-            load_partial(gt + 1, s_nx);
-            pair_send(gt + 1, s_nx);
           }
         } else {
           if (alive)
@@ -2061,19 +1981,20 @@ __global__ void __launch_bounds__((Cfg<BF16, MODE, HD, HDV, BIAS>::NTHREADS), 1)
 
 // Merge split partials: for each row, M = max_s m_s, l = sum_s 2^(m_s - M) l_s,
 // out = sum_s 2^(m_s - M) O_s / l, splits that saw no visible key (l_s == 0)
-// skipped.  Grid (rows, ceil(D / 128)); 256 threads: warp w accumulates splits
-// w, w+8, w+16, ... for 128 columns (4 per lane), then the eight warp sums are
-// added in warp order.  The maximum is a warp-shuffle reduction; every sum runs
-// in a fixed order, so a row's result depends only on that row's partials.
+// skipped and a poisoned split (l_s NaN) carried into the row.  Grid (rows,
+// ceil(D / 128)); 256 threads.  Every warp finds M (a warp-shuffle maximum,
+// exact in any order); warp w accumulates splits w, w+8, w+16, ... for 128
+// columns (4 per lane), and the eight warp sums of O and l are added in warp
+// order.  Every sum runs in a
+// fixed order, so a row's result depends only on that row's partials.
 constexpr int kCombineThreads = 256;
 
 template <bool BF16>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
     const float* __restrict__ part_o, const float* __restrict__ part_ml,
     uint16_t* __restrict__ out, long long R, int D, int n_splits) {
-  extern __shared__ float sm[];
-  float* wts = sm;                          // [n_splits] weights, then the total l
-  float4* acc_w = reinterpret_cast<float4*>(sm + ((n_splits + 4) & ~3));  // [8][32]
+  __shared__ float4 acc_w[8][32];
+  __shared__ float l_w[8];
   // Launched as a programmatic dependent of the attention grid: wait until that
   // grid has completed and its partials are visible.
   ptx::griddep_wait();
@@ -2081,63 +2002,67 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(
   const int c0 = blockIdx.y * 128;
   const int t = threadIdx.x, warp = t / 32, lane = t % 32;
   const bool col_ok = c0 + 4 * lane < D;  // head_dim 192: the second block is half full
-  if (warp == 0) {
-    float mx = -INFINITY;
-    for (int s = lane; s < n_splits; s += 32) {
-      const float2 ml = *reinterpret_cast<const float2*>(part_ml + 2 * (s * R + row));
-      if (ml.y > 0.f) mx = fmaxf(mx, ml.x);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    for (int s = lane; s < n_splits; s += 32) {
-      const float2 ml = *reinterpret_cast<const float2*>(part_ml + 2 * (s * R + row));
-      wts[s] = ml.y > 0.f ? ptx::ex2(ml.x - mx) : 0.f;
-    }
-    __syncwarp();
-    if (lane == 0) {
-      float lt = 0.f;
-      for (int s = 0; s < n_splits; ++s)
-        if (wts[s] != 0.f) lt += wts[s] * part_ml[2 * (s * R + row) + 1];
-      wts[n_splits] = lt;
-    }
-  }
-  __syncthreads();
-  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float2* ml_row = reinterpret_cast<const float2*>(part_ml) + row;
   const float* base = part_o + row * D + c0 + 4 * lane;
   const long long split_stride = R * D;
-  // (head_dim 192: lanes past the last column sit the loop out)
-  for (int s0 = warp; col_ok && s0 < n_splits; s0 += 8 * 4) {
-    float4 v[4];
-    float wv[4];
+  // Warp w takes splits w, w + 8, w + 16, ..., U of them a round; the first
+  // round's loads are issued before those of the maximum, so that up to 8U
+  // splits cost one round trip to memory.
+  constexpr int U = 16;
+  float4 v[U];
+  float2 ml[U];
+  auto load_round = [&](int s0) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int s = s0 + 8 * u;
-      wv[u] = s < n_splits ? wts[s] : 0.f;
-      v[u] = wv[u] != 0.f ? *reinterpret_cast<const float4*>(base + s * split_stride)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
+      ml[u] = s < n_splits ? ml_row[s * R] : make_float2(0.f, 0.f);
+      v[u] = (s < n_splits && col_ok) ? *reinterpret_cast<const float4*>(base + s * split_stride)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      a.x = fmaf(wv[u], v[u].x, a.x);
-      a.y = fmaf(wv[u], v[u].y, a.y);
-      a.z = fmaf(wv[u], v[u].z, a.z);
-      a.w = fmaf(wv[u], v[u].w, a.w);
-    }
+  };
+  load_round(warp);
+  float mx = -INFINITY;
+#pragma unroll 4
+  for (int s = lane; s < n_splits; s += 32) {
+    const float2 m = ml_row[s * R];
+    if (m.y > 0.f) mx = fmaxf(mx, m.x);
   }
-  acc_w[warp * 32 + lane] = a;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lsum = 0.f;
+  for (int s0 = warp;;) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (!(ml[u].y <= 0.f)) {  // saw a key, or poisoned (NaN)
+        const float wv = ptx::ex2(ml[u].x - mx);
+        a.x = fmaf(wv, v[u].x, a.x);
+        a.y = fmaf(wv, v[u].y, a.y);
+        a.z = fmaf(wv, v[u].z, a.z);
+        a.w = fmaf(wv, v[u].w, a.w);
+        lsum = fmaf(wv, ml[u].y, lsum);
+      }
+    }
+    s0 += 8 * U;
+    if (s0 >= n_splits) break;
+    load_round(s0);
+  }
+  acc_w[warp][lane] = a;
+  if (lane == 0) l_w[warp] = lsum;
   __syncthreads();
   if (warp == 0) {
-    float4 sum = acc_w[lane];
+    float4 sum = acc_w[0][lane];
+    float lt = l_w[0];
 #pragma unroll
     for (int w = 1; w < 8; ++w) {
-      const float4 b = acc_w[w * 32 + lane];
+      const float4 b = acc_w[w][lane];
       sum.x += b.x;
       sum.y += b.y;
       sum.z += b.z;
       sum.w += b.w;
+      lt += l_w[w];
     }
-    const float lt = wts[n_splits];
-    const float inv = lt > 0.f ? 1.f / lt : 0.f;
+    const float inv = lt > 0.f ? 1.f / lt : (lt == lt ? 0.f : lt);
     uint2 o;
     o.x = pack2(sum.x * inv, sum.y * inv, BF16);
     o.y = pack2(sum.z * inv, sum.w * inv, BF16);

@@ -22,10 +22,10 @@ using gbsdpa::Cfg;
 // (192, 256).
 template <bool BF16, int MODE, int HD, int HDV, bool BIAS>
 constexpr int variant_index() {
-  return (BIAS ? 48 : 0) + (BF16 ? 1 : 0) +
+  return (BIAS ? 2 * 4 * gbsdpa::kNumModes : 0) + (BF16 ? 1 : 0) +
          2 * (MODE * 4 + (HD != HDV ? 3 : HD == 256 ? 0 : HD == 128 ? 1 : 2));
 }
-constexpr int kNumVariants = 2 * 2 * 6 * 4;
+constexpr int kNumVariants = 2 * 2 * gbsdpa::kNumModes * 4;
 
 struct DeviceState {
   bool ready = false;
@@ -45,7 +45,9 @@ struct DeviceState {
 
 static_assert(variant_index<false, gbsdpa::kSingle, 192, 256, false>() !=
                       variant_index<false, gbsdpa::kSingle, 192, 192, false>() &&
-                  variant_index<true, gbsdpa::kDuoQ, 192, 256, true>() < kNumVariants,
+                  variant_index<true, gbsdpa::kPairXD, 192, 256, false>() <
+                      variant_index<false, gbsdpa::kSingle, 256, 256, true>() &&
+                  variant_index<true, gbsdpa::kPairXD, 192, 256, true>() < kNumVariants,
               "distinct slots within the tables");
 
 template <bool BF16, int MODE, int HD, int HDV, bool BIAS>
@@ -186,11 +188,11 @@ int launch_variant(int mode, int D, int Dv, const AttnParams& p, long long items
                    cudaStream_t stream, DeviceState* st) {
   using gbsdpa::kDuo;
   using gbsdpa::kDuoQ;
-  using gbsdpa::kPair;
   using gbsdpa::kSingle;
   switch (mode) {
-    case kPair: return launch_attn<BF16, kPair, 256, 256, BIAS>(p, items, stream, st);
     case gbsdpa::kPairX: return launch_attn<BF16, gbsdpa::kPairX, 256, 256, BIAS>(p, items, stream, st);
+    case gbsdpa::kPairXD:
+      return launch_attn<BF16, gbsdpa::kPairXD, 256, 256, BIAS>(p, items, stream, st);
     case kDuoQ:
       if constexpr (!BIAS)
         return launch_attn<BF16, kDuoQ, 256, 256, false>(p, items, stream, st);
