@@ -84,7 +84,7 @@ def peaks():
 
 # ---------------------------------------------------------------- ncu traffic
 
-TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "attn_fwd_duo_longkv_gqa_prefill_hd256.txt")
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "attn_fwd_duoq_longkv_gqa_prefill_hd256.txt")
 
 
 def strip_comments(src: str) -> str:
@@ -228,6 +228,52 @@ def time_calls(fn, steps, warmup, flush, stream):
     return [a.elapsed_time(b) for a, b in ev]
 
 
+L2_BYTES = 129 << 20
+
+
+def steady_decode(gb, w, q, k, v, out, ws, cap_bytes=40 << 30):
+    """Per-call device time (ms) of a decode loop's steady state: back-to-back
+    calls captured in one CUDA graph over n rotating copies of K/V, no flush in
+    between; the copies are chosen so that the bytes the n calls read add up
+    to more than 3x L2 (every call reads keys no recent call has touched).
+    Returns (ms, n)."""
+    kvb = decode_bytes(w)
+    per = (k.numel() + v.numel()) * k.element_size()
+    n = max(2, min(64, (3 * L2_BYTES) // max(1, kvb) + 1))
+    n = max(2, min(n, cap_bytes // max(1, per)))
+    ks = [k] + [k.clone() for _ in range(n - 1)]
+    vs = [v] + [v.clone() for _ in range(n - 1)]
+
+    def call(i):
+        gb.sdpa_decode(q, ks[i], vs[i], out, scale=w.scale, causal=w.causal, window=w.window,
+                       workspace=ws)
+
+    torch.cuda.synchronize()
+    cs = torch.cuda.Stream()  # graphs are captured on a stream of their own
+    with torch.cuda.stream(cs):
+        for i in range(n):
+            call(i)
+        cs.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cs):
+            for i in range(n):
+                call(i)
+        g.replay()
+        cs.synchronize()
+        ts = []
+        for _ in range(10):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(cs)
+            g.replay()
+            b.record(cs)
+            cs.synchronize()
+            ts.append(a.elapsed_time(b) / n)
+    torch.cuda.synchronize()
+    del g, ks, vs
+    return statistics.median(ts), n
+
+
 # ---------------------------------------------------------------- CPU baseline (oracle)
 
 def cpu_baseline(w, q, k, v, budget_s=12.0, max_rows=None):
@@ -297,9 +343,15 @@ def suite(gb, device, flush, stream, hbm, bf16_peak):
             ts = time_calls(fn, 20, 5, flush, stream)
             ms = statistics.median(ts)
             gbs = decode_bytes(w) / ms / 1e6
+            sms, ncopy = steady_decode(gb, w, q, k, v, out, ws)
+            sgbs = decode_bytes(w) / sms / 1e6
             res[f"{w.name}_Lq{Lq}"] = {"us": round(ms * 1e3, 2), "GBps": round(gbs, 1),
                                        "frac_of_hbm": round(gbs / hbm, 4),
-                                       "bytes": decode_bytes(w)}
+                                       "bytes": decode_bytes(w),
+                                       "steady_us": round(sms * 1e3, 2),
+                                       "steady_GBps": round(sgbs, 1),
+                                       "steady_frac_of_hbm": round(sgbs / hbm, 4),
+                                       "steady_copies": ncopy}
             del q, k, v, out, ws
             torch.cuda.empty_cache()
     # additive bias (mask array): one [Lq, Lk] mask shared by all heads in prefill,
@@ -374,6 +426,11 @@ def profile_run(args):
     w = table[name]
     if lq is not None:
         w = w.with_(Lq=int(lq))
+    if args.profile_len:
+        # a shorter case of the same kernel: Lk = N, and Lq = N when the
+        # workload's queries span all of its keys
+        n_len = args.profile_len
+        w = w.with_(Lk=n_len, Lq=n_len if w.Lq == w.Lk else min(w.Lq, n_len))
     q, k, v = wl.make_qkv(w, device="cuda")
     out = torch.empty_like(q)
     bias = None
@@ -399,7 +456,7 @@ def profile_run(args):
         fn()
     torch.cuda.synchronize()
     st = gb.device_status()
-    print(json.dumps({"profile": w.name, "Lq": w.Lq, "bias": with_bias,
+    print(json.dumps({"profile": w.name, "Lq": w.Lq, "Lk": w.Lk, "bias": with_bias,
                       "calls": args.warmup + args.steps,
                       "device_status": st[0]}))
     return 0 if st[0] == 0 else 1
@@ -524,6 +581,9 @@ def main():
                     help="run one named workload --steps times (for ncu) and exit; decode "
                          "workloads take a _LqN suffix, and a _bias suffix adds the suite's "
                          "additive bias")
+    ap.add_argument("--profile-len", type=int, default=0,
+                    help="with --profile: run the workload at Lk = N (and Lq = N when its "
+                         "queries span all keys), for a smaller capture of the same kernel")
     ap.add_argument("--routing", action="store_true",
                     help="fused vs unfused (cuBLAS matmul + softmax + matmul) prefill time over "
                          "kL, one JSON line, and exit")
@@ -628,6 +688,10 @@ def main():
     if rank == 0 and not args.no_suite:
         del hq, hk, hv, hout
         line["suite"] = suite(gb, device, flush, stream, hbm, bf16_peak)
+        line["suite_timing"] = ("ms / us: median CUDA-event time of one call, L2 flushed "
+                                "(512 MiB write) before each; decode steady_us: per-call time "
+                                "of back-to-back calls in one CUDA graph over rotating K/V "
+                                "copies (more than 3x L2 read per pass), no flush")
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
