@@ -1155,11 +1155,12 @@ __global__ void __launch_bounds__((Cfg<BF16, MODE, HD, HDV, BIAS>::NTHREADS), 1)
     }
   }
   if constexpr (C::DEC) {
-    // The softmax warps' cluster merge: this warpgroup takes part in its two
-    // cluster barriers (every thread of the cluster arrives at each).
+    // The softmax warps' cluster merge: this warpgroup takes part in its
+    // cluster barriers (every thread of the cluster arrives at each; the
+    // second one is waited for at teardown).
     __syncwarp();
     ptx::cluster_sync();
-    ptx::cluster_sync();
+    ptx::cluster_arrive();
   }
   } else if (C::PX && warp >= C::kExchangeWarp) {
     ptx::setmaxnreg_dec<C::kRegsExchange>();
@@ -1170,9 +1171,8 @@ __global__ void __launch_bounds__((Cfg<BF16, MODE, HD, HDV, BIAS>::NTHREADS), 1)
     // them in XS once our softmax warps and the peer's have read the slot's
     // previous tile, and bulk-copy each warp's block into the peer's X slot.
     // One thread posts the bytes the peer sends into our X slot.  The softmax
-    // warps add the halves.  (One slot: shared memory goes to an 8-slot ring,
-    // which keeps more of a decode's K/V loads in flight; two slots measured
-    // no faster in prefill.)
+    // warps add the halves.  (kPairXD keeps one exchange slot, so that its
+    // shared memory holds an 8-slot ring; kPairX keeps two.)
     const int q4 = warp & 3;
     const int t = q4 * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
@@ -1865,13 +1865,12 @@ __global__ void __launch_bounds__((Cfg<BF16, MODE, HD, HDV, BIAS>::NTHREADS), 1)
       ptx::cluster_sync();  // all partials and abort flags of the cluster are in place
       const int CS = p.dec_cs;
       const uint32_t crank = ptx::cluster_ctarank();
+      // The abort flags are requested here and tested after the partials'
+      // loads have been issued, so that both cost one round trip.
       uint32_t aborted[kMaxDecodeClusterCtas];
 #pragma unroll
       for (int r = 0; r < kMaxDecodeClusterCtas; ++r)
         aborted[r] = r < CS ? ptx::ld_cluster_u32(ptx::mapa(sbase + C::BAR_OFF + 244, r)) : 0u;
-      bool bad = false;
-#pragma unroll
-      for (int r = 0; r < kMaxDecodeClusterCtas; ++r) bad |= aborted[r] != 0u;
       const Work w = make_work<BN, QROWS>(p, item, 0);
       const int ncol = C::DV / CS;
       const int nch = ncol >> 2;
@@ -1899,6 +1898,9 @@ __global__ void __launch_bounds__((Cfg<BF16, MODE, HD, HDV, BIAS>::NTHREADS), 1)
 #pragma unroll
         for (int r = 0; r < kMaxDecodeClusterCtas; ++r)
           if (r < CS) o[r] = ptx::ld_cluster_f4(ptx::mapa(oa, r));
+        bool bad = false;
+#pragma unroll
+        for (int r = 0; r < kMaxDecodeClusterCtas; ++r) bad |= aborted[r] != 0u;
         float M = -INFINITY;
 #pragma unroll
         for (int r = 0; r < kMaxDecodeClusterCtas; ++r)
@@ -1932,7 +1934,9 @@ __global__ void __launch_bounds__((Cfg<BF16, MODE, HD, HDV, BIAS>::NTHREADS), 1)
         }
       }
       asm volatile("bar.sync 1, 256;" ::: "memory");  // (re)converge before the aligned barrier
-      ptx::cluster_sync();  // no CTA reads another's shared memory after this
+      // This CTA has read what it needs from the others' shared memory; the
+      // matching wait, before any CTA of the cluster exits, is at teardown.
+      ptx::cluster_arrive();
     }
   }
 
@@ -1969,6 +1973,9 @@ __global__ void __launch_bounds__((Cfg<BF16, MODE, HD, HDV, BIAS>::NTHREADS), 1)
   // The peer may still write into our shared memory (PAIR) or read our tiles and
   // tensor memory through 2-SM MMAs (DUO) until both CTAs get here.
   if (CLUSTER) ptx::cluster_sync();
+  // Decode: the other CTAs of the cluster may still read this one's partials
+  // until all of them have arrived after the merge.
+  if (C::DEC) ptx::cluster_wait();
   if (warp == C::kMmaWarp) {
     ptx::tc_fence_after();
     if constexpr (DUO)
