@@ -1504,12 +1504,26 @@ __global__ void __launch_bounds__((Cfg<BF16, MODE, HD, HDV, BIAS>::NTHREADS), 1)
         const bool edge = (tb + BN > p.Lk) || (p.causal && tb + BN - 1 > w.pmin) ||
                           (p.causal && p.window && tb < w.pmax - p.window + 1);
         if (edge) {
+          if constexpr (PAIR) {
+            // (The pairs keep the per-key test: the range form below measured
+            // 20% slower in their prefill, through code generation alone.)
 #pragma unroll
-          for (int e = 0; e < HB; ++e) {
-            const int kj = kb + e;
-            const bool vis = kj < p.Lk && (!p.causal || kj <= row_p) &&
-                             (!p.window || row_p - kj < p.window);
-            s[e] = vis ? s[e] : -INFINITY;
+            for (int e = 0; e < HB; ++e) {
+              const int kj = kb + e;
+              const bool vis = kj < p.Lk && (!p.causal || kj <= row_p) &&
+                               (!p.window || row_p - kj < p.window);
+              s[e] = vis ? s[e] : -INFINITY;
+            }
+          } else {
+            // Key kb + e is visible iff lo <= e <= hi: below Lk, at or before
+            // the row's position (causal), and within the window (a window
+            // implies causal).
+            int hi = p.Lk - 1;
+            if (p.causal) hi = min(hi, row_p);
+            const int lo = p.window ? row_p - p.window + 1 - kb : -kb;
+            hi -= kb;
+#pragma unroll
+            for (int e = 0; e < HB; ++e) s[e] = (e >= lo && e <= hi) ? s[e] : -INFINITY;
           }
         }
         // Pair with a bias: the summed scores move to the log2 domain here (-inf,
