@@ -51,6 +51,8 @@ PREFILL_CASES = [
     (1, 2, 2, 513, 65, 256, False, 0),      # query rows spill into a third 256-row tile
     (3, 4, 4, 257, 1000, 256, True, 0),     # batch 3, one row past a 256-row tile
     (1, 2, 1, 256, 3000, 512, True, 0),     # long keys at head_dim 512
+    (1, 4, 2, 600, 1500, 256, True, 300),   # 2-SM window >= 256, head-paired tiles, ragged
+    (1, 3, 1, 400, 900, 256, True, 256),    # 2-SM window, odd group size (256-row tiles)
     # head_dim 192 (one-CTA variant) and 128 (2-SM variant, one CTA for short windows)
     (1, 2, 1, 128, 128, 192, True, 0),
     (1, 4, 2, 200, 333, 192, True, 0),
