@@ -11,16 +11,17 @@
 //     out[h, i] = sum_j softmax_j(scale * q_i . k_j) v_j
 //
 // One CTA owns 128 query rows (one tcgen05 M=128 tile; 256 rows per CTA pair
-// in the 2-SM variant) and walks a list of key tiles.  Warp roles (384
-// threads):
+// in the 2-SM variants) and walks a list of key tiles.  Warp roles (384
+// threads; the head-dim-split pairs add four exchange warps, see Cfg):
 //   warps 0-7  softmax + epilogue: two threads per row / TMEM lane, warps q
 //              and q+4 owning the two halves of the key (and O) columns
 //   warp  8    TMA producer: Q, then K and V sub-tiles into a ring
 //   warp  9    TMEM allocator and tcgen05.mma issuer
 //   warps 10-11 idle (they complete the third warpgroup of the register split)
-// Per key tile j:  S_j = Q K_j^T (tcgen05, fp32 in TMEM, double buffered)
+// Per key tile j:  S_j = Q K_j^T (tcgen05, fp32 in TMEM)
 //                  softmax warps: tcgen05.ld S_j, mask, online max/sum (log2
-//                  domain, lazy rescale), P_j -> shared memory (fp16/bf16)
+//                  domain, lazy rescale), P_j (fp16/bf16) to tensor memory
+//                  over S_j, or to shared memory (kDuoQ and the pairs)
 //                  O += P_j V_j  (tcgen05, fp32 in TMEM)
 // Whole key tiles outside the causal/window band are never visited.  With
 // BIAS, an additive bias (a mask array) is added to the scaled scores.
@@ -38,10 +39,11 @@
 //    depend on how many query rows share the call ("fix: Gemma 4 MTP never
 //    engages on CUDA (GB10)", sections "Proposed Solution" and "Acceptance
 //    Criteria": a verify row must be byte-identical to the single-row call).
-//  * PAIR (head_dim 512): a 2-CTA cluster splits the head dimension; each CTA
-//    forms its half of the scores, the halves are swapped through distributed
-//    shared memory and summed (both CTAs add the same two fp32 numbers, so
-//    both run an identical softmax), then each CTA accumulates its half of O.
+//  * PAIR (head_dim 512, kPairX / kPairXD): a 2-CTA cluster splits the head
+//    dimension; each CTA forms its half of the scores, the halves are swapped
+//    through distributed shared memory and summed (both CTAs add the same two
+//    fp32 numbers, so both run an identical softmax), then each CTA
+//    accumulates its half of O.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -136,7 +138,8 @@ struct AttnParams {
 };
 
 // Kernel variants.
-//   kSingle: one CTA per 128 query rows, head_dim 256 (decode, and prefill fallback).
+//   kSingle: one CTA per 128 query rows: prefill at head_dim 192 (and Q/K 192
+//            with V 256), and prefill with a window under 256 keys.
 //   kDuo:    head_dim 256 prefill with 2-SM MMAs (cta_group::2): a 2-CTA
 //            cluster owns 256 query rows; each CTA loads half of every K and V
 //            tile, which halves the bytes each SM stages per FLOP.
